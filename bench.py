@@ -1,0 +1,495 @@
+"""Benchmark: verified tree tokens/s of the target-verify round on GB300.
+
+One step = one full verify round (tv_build_ancestor_mask, tv_branch_compress, tv_tree_verify_attn,
+tv_accept_walk, tv_refresh_commit) over one batch of synthetic requests.  Default workload: the
+serving batch -- 64 requests with ragged prefixes U{1024..8192}, C4 + C128 + 128-token window,
+64 query heads sharing one KV head, head dim 512, bf16, top-2 draft trees pruned to D = 8.
+
+value  = whole-job verified tree tokens per second (sum over ranks of B * D per step / max time).
+e2e    = the same metric through the C ABI with the round's inputs copied from pinned host memory
+         and its outputs copied back inside the timed region.
+roofline, hbm = the attention kernel's algorithmic flops / bytes per launch over its CUDA-event
+         duration, against the measured peaks.
+cpu_baseline = the fp64 CPU oracle on a bounded sample of the same workload (rank 0, N = 1).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--workload serving|small|long|tiny] [--no-cpu-baseline]
+Multi-GPU: launched by torchrun, one rank per GPU; each rank verifies its own batch (requests are
+independent: replicas with no data-path collective, weak scaling).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_SETS = 3   # rotating copies of the state: each step touches data last used 3 steps earlier
+WORKLOAD_DESC = {
+    "serving": "serving batch: B=64, L~U{1024..8192}, D=8 (top-2 tree, 4 steps), H=64x1, d=512, "
+               "C4+C128+W128, bf16",
+    "small": "small: B=4, L=4096, D=6 (top-2, depth 3), H=64x1, d=512, C4+C128+W128, bf16",
+    "long": "long context: B=8, L~U{65536..131072}, C128 + top-2048 C4, W128, D=8, H=64x1, "
+            "d=512, bf16",
+    "tiny": "tiny fp32: B=1, L=256, C4 only, remainder tail, D=5, H=8x1, d=64",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOAD_DESC), default="serving")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-kernel", choices=["auto", "simt", "tcgen05"], default="auto")
+    return ap.parse_args()
+
+
+def make_workload(name, rank):
+    from tree_speculative_verify_gb300 import workloads
+    seed = rank
+    if name == "serving":
+        return workloads.serving(seed=seed)
+    if name == "small":
+        return workloads.small(seed=seed)
+    if name == "long":
+        return workloads.long_context(seed=seed)
+    return workloads.tiny(seed=seed)
+
+
+# ---- accounting (host-side, from the workload's integers) -------------------------------------
+
+def visible_counts(wl):
+    """Per request and node: how many entries the node attends to, and the tail entries and
+    scratch rows the round reads.  Pure bookkeeping for the roofline numerators."""
+    out = []
+    for b in range(wl.B):
+        L = int(wl.L[b])
+        par = [int(x) for x in wl.parents[b]]
+        depth = [0] * wl.D
+        for v in range(1, wl.D):
+            depth[v] = depth[par[v]] + 1
+        n4 = (wl.n_sel if wl.n_sel else L // 4) if 4 in wl.ms else 0
+        n128 = L // 128 if 128 in wl.ms else 0
+        closes = {m: [(L + depth[v] + 1) % m == 0 for v in range(wl.D)] for m in wl.ms}
+        n_scr = sum(sum(c) for c in closes.values())
+        m_min = 4 if 4 in wl.ms else 128
+        per_node = []
+        for v in range(wl.D):
+            p = L + depth[v]
+            lo = max(0, p - wl.W) if wl.tail_mode == "window" else m_min * (p // m_min)
+            anc = []
+            u = v
+            while True:
+                anc.append(u)
+                if u == 0:
+                    break
+                u = par[u]
+            n_tree = sum(1 for u in anc if L + depth[u] >= lo)
+            n_scr_v = sum(1 for m in wl.ms for u in anc if u != v and closes[m][u])
+            per_node.append(n4 + n128 + max(0, L - lo) + n_tree + n_scr_v)
+        tail = min(L, wl.W) if wl.tail_mode == "window" else L - m_min * (L // m_min)
+        out.append(dict(shared=n4 + n128, tail=tail, tree=wl.D, scr=n_scr, per_node=per_node))
+    return out
+
+
+def attention_accounting(wl):
+    es = 2 if wl.dtype == "bf16" else 4
+    counts = visible_counts(wl)
+    kv_bytes = sum((c["shared"] + c["tail"] + c["tree"] + c["scr"]) * 2 * wl.d * es for c in counts)
+    qo_bytes = 2 * wl.B * wl.D * wl.H * wl.d * es
+    flops = sum(4 * wl.d * wl.H * n for c in counts for n in c["per_node"])
+    return kv_bytes, qo_bytes, flops
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], tc=p["bf16_tflops"], tc_sus=p["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sus=1700.0, source="fallback")
+
+
+def traffic_record(kernel_name):
+    """DRAM bytes per launch from a committed ncu summary, valid only for the source it measured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    entry = rec.get(kernel_name)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "tree_speculative_verify_gb300", "csrc", entry["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != entry["source_sha256_16"]:
+        return None
+    return entry
+
+
+# ---- clocks -----------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- distributed ------------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}: launch N>1 with torchrun")
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- the CPU oracle (baseline / reference arm) ------------------------------------------------
+
+def oracle_setup(wl, requests):
+    """Oracle-made compressed prefix of the sampled requests (state preparation, not timed)."""
+    import oracle
+    comp = {}
+    for m in wl.ms:
+        cap = wl.cap4 if m == 4 else wl.cap128
+        CK = np.zeros((wl.B, cap, wl.d), dtype=np.float32)
+        CV = np.zeros((wl.B, cap, wl.d), dtype=np.float32)
+        for b in requests:
+            L = int(wl.L[b])
+            ck, cv = oracle.compress_prefix(wl.rawK[b, :L].float().numpy(),
+                                            wl.rawV[b, :L].float().numpy(), L, m,
+                                            wl.g[m].float().numpy(), wl.dtype)
+            CK[b, :L // m], CV[b, :L // m] = ck, cv
+        comp[m] = (CK, CV)
+    return comp
+
+
+class _Rows:
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, b):
+        return self.t[b].float().numpy()
+
+
+def oracle_round(wl, comp, requests):
+    import oracle
+    cfg = oracle.VerifyConfig(H=wl.H, d=wl.d, ms=wl.ms, W=wl.W, tail_mode=wl.tail_mode,
+                              store=wl.dtype)
+    g = {m: wl.g[m].float().numpy() for m in wl.ms}
+    return oracle.verify_round(cfg, wl.parents, wl.L, _Rows(wl.Q), comp, wl.sel, _Rows(wl.rawK),
+                               _Rows(wl.rawV), _Rows(wl.treeK), _Rows(wl.treeV), g, wl.draft,
+                               wl.target, requests=requests)
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except ImportError:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(wl, budget_s=20.0):
+    """Time the oracle's verify round on requests 0, 1, ... until ~budget_s of CPU work."""
+    order = list(range(wl.B))
+    comp = oracle_setup(wl, order)
+    done, t_total = [], 0.0
+    for b in order:
+        t0 = time.perf_counter()
+        oracle_round(wl, comp, [b])
+        t_total += time.perf_counter() - t0
+        done.append(b)
+        if t_total >= budget_s:
+            break
+    value = len(done) * wl.D / t_total
+    return {"value": value, "unit": "verified tree tokens/s", "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle, one verify round of {len(done)} of the {wl.B} requests "
+                      f"(same workload, same seed), {t_total:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    from tree_speculative_verify_gb300 import workloads  # noqa: F401  (inputs only)
+    if rank != 0:
+        return
+    wl = make_workload(args.workload, 0)
+    per_step = max(1, min(wl.B, 4))
+    reqs = [list(range(i * per_step % wl.B, i * per_step % wl.B + per_step)) for i in range(
+        args.warmup + args.steps)]
+    reqs = [[b % wl.B for b in r] for r in reqs]
+    comp = oracle_setup(wl, sorted({b for r in reqs for b in r}))
+    for i in range(args.warmup):
+        oracle_round(wl, comp, reqs[i])
+    t0 = time.perf_counter()
+    tokens = 0
+    for i in range(args.steps):
+        r = reqs[args.warmup + i]
+        oracle_round(wl, comp, r)
+        tokens += len(r) * wl.D
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    line = {
+        "impl": "reference", "metric": "verified tree tokens/s", "value": value,
+        "unit": "verified tree tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "B": wl.B, "D": wl.D,
+                   "sample_per_step": f"{per_step} requests"},
+        "cpu_baseline": {"value": value, "unit": "verified tree tokens/s", "cores": cpu_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} requests of the workload per step"},
+        "e2e": {"value": value, "unit": "verified tree tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm ------------------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    from tree_speculative_verify_gb300 import _lib, build as tvbuild, engine
+    tvbuild.build()
+    kernel = {"auto": _lib.TV_ATTN_AUTO, "simt": _lib.TV_ATTN_SIMT,
+              "tcgen05": _lib.TV_ATTN_TCGEN05}[args.attn_kernel]
+    wl = make_workload(args.workload, rank)
+    shape = engine.shape_for(wl, kernel)
+    stream = torch.cuda.current_stream()
+    sets = []
+    for _ in range(N_SETS):
+        st = engine.alloc_state(wl)
+        rb = engine.alloc_round(wl, shape)
+        engine.prefill(shape, st, rb, stream)
+        sets.append((st, rb, st.L.clone()))
+    torch.cuda.synchronize()
+    for _, rb, _ in sets:
+        if int(rb.status.item()) != 0:
+            raise SystemExit(f"prefill failed: status {int(rb.status.item())}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+
+    def step(i, timed=None):
+        st, rb, L0 = sets[i % N_SETS]
+        st.L.copy_(L0, non_blocking=True)
+        engine.plan(shape, st, rb, stream)
+        engine.branch_compress(shape, st, rb, stream)
+        if timed is not None:
+            timed[0].record(stream)
+        engine.attention(shape, st, rb, None, stream)
+        if timed is not None:
+            timed[1].record(stream)
+        engine.accept(shape, st, rb, stream)
+        engine.refresh(shape, st, rb, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + k, ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    barrier(world)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms, world)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    for _, rb, _ in sets:
+        if int(rb.status.item()) != 0:
+            raise SystemExit(f"device status {int(rb.status.item())} after the timed steps")
+
+    # end to end through the C ABI: inputs from pinned host memory, outputs back to the host
+    st, rb, L0 = sets[0]
+    ins = [rb.Q, rb.treeK, rb.treeV, rb.parents, rb.draft, rb.target]
+    outs = [rb.O, rb.lse, rb.accept_len, rb.path, rb.bonus, rb.committed]
+    host_in = [t.cpu().pin_memory() for t in ins]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def e2e_step(i):
+        s_, r_, l_ = sets[i % N_SETS]
+        s_.L.copy_(l_, non_blocking=True)
+        for dst, src in zip([r_.Q, r_.treeK, r_.treeV, r_.parents, r_.draft, r_.target], host_in):
+            dst.copy_(src, non_blocking=True)
+        engine.verify_round(shape, s_, r_, None, stream)
+        for dst, src in zip(host_out, [r_.O, r_.lse, r_.accept_len, r_.path, r_.bonus, r_.committed]):
+            dst.copy_(src, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    barrier(world)
+
+    tokens_per_step = world * wl.B * wl.D
+    value = tokens_per_step / (ms * 1e-3)
+    kv_bytes, qo_bytes, flops = attention_accounting(wl)
+    pk = peaks()
+    attn_s = attn_ms * 1e-3
+    tc_name = "tcgen05" if _lib.tv_attn_kernel_for(shape) == _lib.TV_ATTN_TCGEN05 else "simt"
+    traffic = traffic_record(f"attention_{tc_name}_{args.workload}")
+    tflops = flops / attn_s / 1e12
+    gbs = kv_bytes / attn_s / 1e9
+    line = {
+        "metric": "verified tree tokens/s and achieved HBM GB/s (% of peak), D=8 bs=64, 1 GB300",
+        "value": value, "unit": "verified tree tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "B_per_gpu": wl.B, "D": wl.D,
+                   "H": wl.H, "d": wl.d, "attention_kernel": tc_name,
+                   "l2": f"inputs larger than L2: {N_SETS} rotating state copies, "
+                         f"{kv_bytes / 1e6:.0f} MB KV per step each",
+                   "parallelism": f"replicas x{world} (requests sharded, no collective)"},
+        "roofline": {"bound": "tensor", "achieved": tflops,
+                     "peak": pk["tc_sus"], "unit": "TFLOP/s", "frac": tflops / pk["tc_sus"],
+                     "traffic": None if traffic is None else traffic["bytes_per_launch"],
+                     "kernel": f"tv_tree_verify_attn ({tc_name})",
+                     "peak_source": f"{pk['source']} bf16 dense, sustained",
+                     "algorithmic_flops_per_launch": flops},
+        "hbm": {"achieved": gbs, "peak": pk["hbm"], "unit": "GB/s", "frac": gbs / pk["hbm"],
+                "frac_of_8TBps": gbs / 8000.0, "algorithmic_bytes_per_launch": kv_bytes,
+                "with_q_and_o_bytes": kv_bytes + qo_bytes,
+                "note": "compressed KV + raw tail + tree + scratch rows, read once per request"},
+        "attention_ms": attn_ms,
+        "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "verified tree tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * launches_per_step(shape, tc_name),
+        "clocks": clk,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def launches_per_step(shape, kernel):
+    # plan, branch compress, attention (+ merge), accept, refresh
+    return 4 + (2 if kernel == "simt" else 2)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+/*
+ * treeverify.h -- C ABI of libtreeverify.so: the target-verify hot path of tree-structured
+ * speculative decoding over online-compressed (C4 / C128) attention, for NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for
+ * Efficient Inference" (arXiv 2609.24698), cited as [TSD-V4] with inferred section numbers
+ * (§2.2 CSA/HCA compression, §3.1 branch-aware causality, §3.2 isolation, §4.1 three-stage
+ * forward and verification plan, §4.2 scratch pad and refresh, §4.3 optimisations, §5.1 naming).
+ *
+ * One verify round is five calls on one stream, with no host synchronisation in between:
+ *   tv_build_ancestor_mask -> tv_branch_compress -> tv_tree_verify_attn -> tv_accept_walk
+ *   -> tv_refresh_commit
+ * plus tv_prefill_compress, which builds the persistent compressed prefix of a fresh batch.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller (unless stated otherwise).
+ *   The library allocates nothing; scratch space for the attention is the caller's workspace.
+ * - Every call is asynchronous on the cudaStream_t it is given (0 = legacy default stream) and
+ *   returns TV_OK once its kernels are enqueued, or a negative TV_ERR_* code, without launching
+ *   anything, when the host-side arguments are invalid (null pointer, bad shape).  The reason of
+ *   the last host-side error of the calling thread is available from tv_last_error_string().
+ * - Errors found on the device (a malformed tree, a capacity overflow, a bad selection index,
+ *   a wait that ran out) are written to the caller's int32 *status word with first-error-wins
+ *   semantics (the word is only ever changed from 0 to a negative code); read it after the
+ *   stream has been synchronised.  The affected request's outputs are then unspecified, the
+ *   other requests' outputs are valid.  Kernels never trap and every wait is bounded.
+ * - Tree: node 0 is the root, the last accepted token, whose K/V and query are produced in this
+ *   pass; parents[b][0] == -1 and 0 <= parents[b][v] < v (topological numbering); D counts the
+ *   root ([TSD-V4] §5.1: s4_k1_d5 verifies 4 draft tokens plus the root with budget 5).
+ *   Node v of request b sits at position L[b] + depth[b][v].
+ * - Persistent state of request b (row-major, row length d elements, dtype of the shape):
+ *     rawK/rawV  [B][raw_cap][d]   raw per-token K/V, rows 0 .. L[b]-1 committed
+ *     c4K/c4V    [B][c4_cap][d]    C4 entries, rows 0 .. L[b]/4 - 1 valid
+ *     c128K/V    [B][c128_cap][d]  C128 entries, rows 0 .. L[b]/128 - 1 valid
+ *     L          [B] int32         committed length
+ *   The number of valid compressed entries is always floor(L / m): there is no separate count.
+ *   Rows beyond the valid ones are never read for their values but may be loaded; they must hold
+ *   finite numbers (allocate the buffers zero-filled).
+ * - Scratch pad ([TSD-V4] §4.2): scrK4/scrV4 and scrK128/scrV128 [B][D][d], one row per tree
+ *   node; row v holds the compressed entry of the block that node v's token closes, or zeros.
+ *   It is separate from the persistent state, which only tv_refresh_commit writes.
+ * - Compressor m (4 = C4, 128 = C128): block j covers positions m*j .. m*j+m-1; gate logit of
+ *   token t is z_t = K_t . g_m (no scale); w = softmax(z) over the block; the entry is
+ *   (sum_t w_t K_t, sum_t w_t V_t), computed in fp32 and stored in the cache dtype (round to
+ *   nearest even).  [TSD-V4] §2.2 gives no formula; this gated block sum is the fixed stand-in.
+ * - Visibility ([TSD-V4] §3.1, §3.2): a query at position p sees compressed entry (m, j) iff
+ *   m*j+m-1 <= p-1, and raw tokens at positions raw_lo(p) .. p; a tree node sees only its own
+ *   ancestors (and itself) among the tree tokens and only its proper ancestors' scratch entries.
+ *   raw_lo(p) = max(0, p - W) (TV_TAIL_WINDOW) or m_min * floor(p / m_min) (TV_TAIL_REMAINDER,
+ *   m_min = 4 if C4 is active, else 128).
+ */
+#ifndef TREEVERIFY_H
+#define TREEVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tv_stream_t; /* the same handle type as cudaStream_t */
+
+/* status codes */
+#define TV_OK 0
+#define TV_ERR_ARG (-1)        /* null pointer, unknown enum value or inconsistent argument */
+#define TV_ERR_SHAPE (-2)      /* unsupported shape (D > 64, d not a multiple of 8, ...) */
+#define TV_ERR_BAD_TREE (-3)   /* parents[b][0] != -1 or parents[b][v] not in [0, v) */
+#define TV_ERR_CAPACITY (-4)   /* a length or entry count exceeds the buffer capacity */
+#define TV_ERR_DTYPE (-5)      /* dtype not supported by the requested kernel */
+#define TV_ERR_CUDA (-6)       /* a CUDA runtime call failed (launch, tensor-map encoding) */
+#define TV_ERR_WORKSPACE (-7)  /* workspace too small (see tv_workspace_size) */
+#define TV_ERR_TIMEOUT (-8)    /* a bounded device-side wait ran out (kernel returned early) */
+#define TV_ERR_SELECTION (-9)  /* a selection index is outside the request's C4 entries */
+
+/* tv_shape.tail_mode */
+#define TV_TAIL_WINDOW 0
+#define TV_TAIL_REMAINDER 1
+/* tv_shape.comp_mask bits */
+#define TV_COMP_C4 1
+#define TV_COMP_C128 2
+/* tv_shape.dtype */
+#define TV_F32 0
+#define TV_BF16 1
+/* tv_shape.attn_kernel */
+#define TV_ATTN_AUTO 0    /* tensor-core kernel where supported, else the SIMT kernel */
+#define TV_ATTN_SIMT 1    /* CUDA-core fp32 kernel: any supported shape, fp32 or bf16 */
+#define TV_ATTN_TCGEN05 2 /* tcgen05 tensor-core kernel: bf16, d == 512 */
+
+typedef struct tv_shape {
+  int32_t B;           /* requests (>= 0; B == 0 turns every call into a no-op) */
+  int32_t D;           /* tree nodes per request including the root, 1..64 */
+  int32_t H;           /* query heads sharing the single K/V head, 1..1024 */
+  int32_t d;           /* head dimension of Q, K, V and O: multiple of 8, 8..512 */
+  int32_t W;           /* raw window for TV_TAIL_WINDOW, 0..1024 (ignored otherwise) */
+  int32_t tail_mode;   /* TV_TAIL_WINDOW | TV_TAIL_REMAINDER */
+  int32_t comp_mask;   /* non-empty subset of TV_COMP_C4 | TV_COMP_C128 */
+  int32_t dtype;       /* TV_F32 | TV_BF16: storage of Q, K, V, O, raw and compressed rows */
+  int32_t n_sel;       /* 0: all persistent C4 entries visible; > 0: only the n_sel listed ones */
+  int32_t attn_kernel; /* TV_ATTN_* */
+  int64_t raw_cap;     /* rows per request of rawK / rawV */
+  int64_t c4_cap;      /* rows per request of c4K / c4V (ignored without C4) */
+  int64_t c128_cap;    /* rows per request of c128K / c128V (ignored without C128) */
+} tv_shape;
+
+/* Library version string (static storage). */
+const char* tv_version(void);
+
+/* Human-readable name of a TV_* status code (static storage). */
+const char* tv_status_string(int code);
+
+/* Description of the calling thread's last host-side error (thread-local storage, valid until
+ * the thread's next call into the library). */
+const char* tv_last_error_string(void);
+
+/* Bytes of device workspace tv_tree_verify_attn needs for this shape (0 for B == 0).  The
+ * workspace holds the split-KV partial results and the work counters; the caller allocates it
+ * (any 256-byte-aligned device buffer) and may reuse it across calls on the same stream. */
+size_t tv_workspace_size(const tv_shape* shape);
+
+/* The attention kernel tv_tree_verify_attn runs for this shape on the current device:
+ * TV_ATTN_SIMT or TV_ATTN_TCGEN05, or a negative TV_ERR_* code for an invalid shape. */
+int tv_attn_kernel_for(const tv_shape* shape);
+
+/*
+ * Verify preprocess: the verification plan ([TSD-V4] §4.1 -- the candidate tree becomes the
+ * metadata that guides attention and compression; §4.3 -- built on the device).
+ *   parents  [B][D] int32   in   tree topology
+ *   L        [B]    int32   in   committed lengths
+ *   anc      [B][D] uint64  out  bit u of anc[b][v] set iff u is on the path root -> v
+ *   depth    [B][D] int32   out  depth of v (root 0); position = L[b] + depth
+ *   raw_lo   [B][D] int32   out  lowest raw position visible from v (see raw_lo(p) above)
+ *   scr_vis4 [B][D] uint64  out  proper ancestors of v whose token closes a C4 block
+ *                                 (nullable when C4 is inactive)
+ *   scr_vis128 [B][D] uint64 out same for C128 (nullable when C128 is inactive)
+ * Device errors: TV_ERR_BAD_TREE (that request's outputs are zero), TV_ERR_ARG for L < 0.
+ */
+int tv_build_ancestor_mask(const tv_shape* shape, const int32_t* parents, const int32_t* L,
+                           uint64_t* anc, int32_t* depth, int32_t* raw_lo, uint64_t* scr_vis4,
+                           uint64_t* scr_vis128, int32_t* status, tv_stream_t stream);
+
+/*
+ * Prefill compression ([TSD-V4] §2.2): writes every complete block of each request's committed
+ * prefix, entries 0 .. floor(L[b]/m) - 1 of each active compressor, from the raw rows.
+ *   rawK, rawV [B][raw_cap][d] in; L [B] in; g4, g128 [d] fp32 gate vectors (nullable when the
+ *   compressor is inactive); c4K, c4V, c128K, c128V out.
+ * Device errors: TV_ERR_CAPACITY when L > raw_cap or floor(L/m) > cap_m (request skipped).
+ */
+int tv_prefill_compress(const tv_shape* shape, const void* rawK, const void* rawV,
+                        const int32_t* L, const float* g4, const float* g128, void* c4K,
+                        void* c4V, void* c128K, void* c128V, int32_t* status,
+                        tv_stream_t stream);
+
+/*
+ * Scratch-pad branch compression ([TSD-V4] §3.2, §4.1, §4.2: a chain that closes a block after
+ * branching is compressed on its own, into temporary storage).  For every node v and active
+ * compressor m with (L[b] + depth(v) + 1) % m == 0, row v of the m scratch pad becomes the gated
+ * sum of the m positions ending at v's position, read from the sequence prefix + path(v):
+ * positions < L[b] from rawK/rawV, the others from treeK/treeV of v's ancestors.  Every other
+ * row is set to zero.
+ *   rawK, rawV [B][raw_cap][d] in; L [B] in; treeK, treeV [B][D][d] in (K/V of the tree tokens);
+ *   parents [B][D] in; g4, g128 [d] fp32 in; scrK4, scrV4, scrK128, scrV128 [B][D][d] out
+ *   (the pair of an inactive compressor is nullable).
+ * Device errors: TV_ERR_BAD_TREE, TV_ERR_CAPACITY (L > raw_cap).
+ */
+int tv_branch_compress(const tv_shape* shape, const void* rawK, const void* rawV,
+                       const int32_t* L, const void* treeK, const void* treeV,
+                       const int32_t* parents, const float* g4, const float* g128, void* scrK4,
+                       void* scrV4, void* scrK128, void* scrV128, int32_t* status,
+                       tv_stream_t stream);
+
+/*
+ * Branch-aware causal tree-verify attention ([TSD-V4] §3.1, §4.1, §4.4), split-KV.
+ * Every (node v, head h) row attends, with logit scale `scale` (normally 1/sqrt(d)), to
+ *   - the persistent C4 entries 0 .. L/4-1 (or, with n_sel > 0, the listed ones sel[b][i]),
+ *   - the persistent C128 entries 0 .. L/128-1,
+ *   - the raw rows at positions raw_lo[b][v] .. L-1,
+ *   - the tree tokens u with anc bit u set and position L + depth(u) >= raw_lo[b][v],
+ *   - the scratch entries of the nodes flagged in scr_vis4 / scr_vis128.
+ * The compressed prefix is read once per request and shared by all D*H rows.
+ *   Q    [B][D][H][d] in (dtype);  sel [B][n_sel] int32 (nullable when n_sel == 0)
+ *   anc, raw_lo, scr_vis4, scr_vis128: the plan of tv_build_ancestor_mask
+ *   O    [B][D][H][d] out (dtype); lse [B][D][H] fp32 out: natural-log sum of exp(logits)
+ *   workspace: device buffer of ws_bytes >= tv_workspace_size(shape)
+ * Host errors: TV_ERR_WORKSPACE, TV_ERR_DTYPE (TV_ATTN_TCGEN05 asked for an unsupported shape).
+ * Device errors: TV_ERR_SELECTION, TV_ERR_CAPACITY, TV_ERR_TIMEOUT.
+ */
+int tv_tree_verify_attn(const tv_shape* shape, const void* Q, const void* c4K, const void* c4V,
+                        const int32_t* sel, const void* c128K, const void* c128V,
+                        const void* rawK, const void* rawV, const int32_t* L,
+                        const void* treeK, const void* treeV, const uint64_t* anc,
+                        const int32_t* raw_lo, const uint64_t* scr_vis4,
+                        const uint64_t* scr_vis128, const void* scrK4, const void* scrV4,
+                        const void* scrK128, const void* scrV128, float scale, void* O,
+                        float* lse, void* workspace, size_t ws_bytes, int32_t* status,
+                        tv_stream_t stream);
+
+/*
+ * Accepted-path selection ([TSD-V4] §3.2, §4.1): greedy walk from the root; at each node take
+ * the lowest-numbered child whose draft token equals the node's target token; stop when none.
+ *   parents, draft, target [B][D] int32 in
+ *   accept_len [B] out: path length including the root (>= 1)
+ *   path [B][D] out: accepted node ids in order, -1 padded
+ *   bonus [B] out: target token of the last accepted node
+ * Device errors: TV_ERR_BAD_TREE.
+ */
+int tv_accept_walk(const tv_shape* shape, const int32_t* parents, const int32_t* draft,
+                   const int32_t* target, int32_t* accept_len, int32_t* path, int32_t* bonus,
+                   int32_t* status, tv_stream_t stream);
+
+/*
+ * Accepted-path state refresh ([TSD-V4] §3.2, §4.2: only the accepted path's token, KV and
+ * compressed states reach the persistent context; rejected branches are dropped).
+ * With n = accept_len[b] and path = path[b]:
+ *   rawK/rawV row L+i <- treeK/treeV row path[i] (exact copy), i < n;
+ *   for every active m and position e in [L, L+n-1] with (e+1) % m == 0: entry (e+1)/m - 1 <-
+ *   scratch row path[e-L] of compressor m (that row is the gated sum of exactly the committed
+ *   block, so the copy equals recompressing it); L[b] <- L + n;
+ *   committed_pos[b][i] = old L + i for i < n, -1 otherwise.
+ * The scratch pad must come from tv_branch_compress of the same round.
+ * Device errors: TV_ERR_CAPACITY (L+n > raw_cap or an entry beyond cap_m; request untouched),
+ * TV_ERR_ARG (accept_len outside 1..D or a path id outside 0..D-1; request untouched).
+ */
+int tv_refresh_commit(const tv_shape* shape, const int32_t* accept_len, const int32_t* path,
+                      const void* treeK, const void* treeV, const void* scrK4,
+                      const void* scrV4, const void* scrK128, const void* scrV128, void* rawK,
+                      void* rawV, void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
+                      int32_t* committed_pos, int32_t* status, tv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol include/treeverify.h declares, and its host-side
+validation rejects bad arguments -- all without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tree_speculative_verify_gb300 import _lib, build as tvbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "treeverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tvbuild.build()
+    return _lib.load()
+
+
+def _declarations():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = {}
+    for m in re.finditer(r"^\s*[\w\s\*]+?\b(tv_\w+)\s*\(([^;]*?)\)\s*;", text, flags=re.M | re.S):
+        args = m.group(2).strip()
+        n = 0 if args in ("", "void") else args.count(",") + 1
+        decls[m.group(1)] = n
+    return decls
+
+
+def test_header_declares_the_entry_points():
+    decls = _declarations()
+    for name in _lib.EXPORTS:
+        assert name in decls, name
+    assert set(decls) == set(_lib.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declarations():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_match_header(lib):
+    decls = _declarations()
+    for name, n in decls.items():
+        assert len(_lib._SIGS[name][0]) == n, (name, len(_lib._SIGS[name][0]), n)
+
+
+def test_version_and_status_strings(lib):
+    assert "treeverify" in _lib.version()
+    assert lib.tv_status_string(-3) == b"TV_ERR_BAD_TREE"
+    assert lib.tv_status_string(0) == b"TV_OK"
+
+
+def test_struct_layout_matches_c():
+    assert ctypes.sizeof(_lib.tv_shape) == 10 * 4 + 3 * 8
+
+
+def _shape(**kw):
+    base = dict(B=2, D=8, H=64, d=512, W=128, raw_cap=1000, c4_cap=260, c128_cap=9)
+    base.update(kw)
+    return _lib.make_shape(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=0), -2), (dict(D=65), -2), (dict(d=12), -2), (dict(d=1024), -2), (dict(H=0), -2),
+    (dict(tail_mode=7), -1), (dict(comp_mask=0), -1), (dict(dtype=3), -1), (dict(B=-1), -2),
+    (dict(n_sel=5, comp_mask=2), -1), (dict(attn_kernel=9), -1), (dict(raw_cap=-1), -2),
+])
+def test_host_validation_rejects_bad_shapes(lib, kw, code):
+    s = _shape(**kw)
+    rc = lib.tv_accept_walk(ctypes.byref(s), None, None, None, None, None, None, None, None)
+    assert rc == code
+    assert lib.tv_last_error_string() != b""
+    assert lib.tv_workspace_size(ctypes.byref(s)) == 0
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    s = _shape()
+    rc = lib.tv_build_ancestor_mask(ctypes.byref(s), None, None, None, None, None, None, None,
+                                    None, None)
+    assert rc == -1 and b"null" in lib.tv_last_error_string()
+    rc = lib.tv_refresh_commit(ctypes.byref(s), *([None] * 18))
+    assert rc == -1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    s = _shape(B=0)
+    assert lib.tv_accept_walk(ctypes.byref(s), None, None, None, None, None, None, None, None) == 0
+    assert lib.tv_workspace_size(ctypes.byref(s)) == 0
+
+
+def test_workspace_size_grows_with_batch(lib):
+    a = lib.tv_workspace_size(ctypes.byref(_shape(B=2)))
+    b = lib.tv_workspace_size(ctypes.byref(_shape(B=4)))
+    assert 0 < a < b and a % 256 == 0

@@ -1,0 +1,322 @@
+// Online sequence compression (C4 / C128), the scratch pad and the accepted-path refresh.
+//
+// "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for Efficient Inference":
+//   §2.2  CSA/HCA compress blocks of positions online, at two granularities (here m = 4, 128);
+//   §3.2  a branch that closes a block after the tree diverges must be compressed on its own;
+//   §4.2  those branch states live in a scratch pad; after acceptance only the accepted path's
+//         raw tokens and compressed entries are committed to the persistent cache.
+//
+// The report gives no compression formula; the library's fixed stand-in is the gated block sum
+//   z_t = K_t . g_m,  w = softmax(z) over the block,  entry = (sum_t w_t K_t, sum_t w_t V_t),
+// evaluated in fp32 and stored in the cache dtype.  All three kernels call the same device
+// routine with the same thread layout, so an entry computed in the scratch pad is bit-identical
+// to the one prefill would compute for the same committed block.
+#include <math.h>
+
+#include "tv_common.cuh"
+
+namespace tv {
+
+constexpr int kCompressThreads = 128;
+
+// One compressed entry from the m token rows rowK[t] / rowV[t] (t in position order).
+// Whole-CTA routine; w_smem holds m floats.  Reduction orders depend only on the warp size.
+template <typename T>
+__device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int m, int d,
+                                const float* __restrict__ g, T* outK, T* outV, float* w_smem) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  for (int t = warp; t < m; t += nwarps) {
+    const T* k = rowK[t];
+    float acc = 0.f;
+    for (int i = lane; i < d; i += 32) acc = fmaf(load_f(k + i), g[i], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) w_smem[t] = acc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float mx = -INFINITY;
+    for (int t = lane; t < m; t += 32) mx = fmaxf(mx, w_smem[t]);
+    mx = warp_max(mx);
+    float s = 0.f;
+    for (int t = lane; t < m; t += 32) {
+      const float e = expf(w_smem[t] - mx);
+      w_smem[t] = e;
+      s += e;
+    }
+    s = warp_sum(s);
+    const float inv = 1.f / s;
+    __syncwarp();
+    for (int t = lane; t < m; t += 32) w_smem[t] *= inv;
+  }
+  __syncthreads();
+  for (int i = tid; i < d; i += blockDim.x) {
+    float ak = 0.f, av = 0.f;
+    for (int t = 0; t < m; ++t) {
+      const float w = w_smem[t];
+      ak = fmaf(w, load_f(rowK[t] + i), ak);
+      av = fmaf(w, load_f(rowV[t] + i), av);
+    }
+    store_f(outK + i, ak);
+    store_f(outV + i, av);
+  }
+}
+
+// ---- prefill: every complete block of the committed prefix ---------------------------------
+// grid.x: entry index (strided), grid.y: request.
+template <typename T>
+__global__ void prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
+                               const T* __restrict__ rawK, const T* __restrict__ rawV,
+                               const int32_t* __restrict__ L, const float* __restrict__ g,
+                               T* __restrict__ CK, T* __restrict__ CV, int32_t* status) {
+  __shared__ const T* rowK[128];
+  __shared__ const T* rowV[128];
+  __shared__ float w[128];
+  const int b = blockIdx.y;
+  const int Lb = L[b];
+  if (Lb < 0 || Lb > raw_cap || (int64_t)(Lb / m) > cap_m) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_error(status, TV_ERR_CAPACITY);
+    return;
+  }
+  const int n = Lb / m;
+  for (int j = blockIdx.x; j < n; j += gridDim.x) {
+    for (int t = threadIdx.x; t < m; t += blockDim.x) {
+      const int64_t row = (int64_t)b * raw_cap + (int64_t)j * m + t;
+      rowK[t] = rawK + row * d;
+      rowV[t] = rawV + row * d;
+    }
+    __syncthreads();
+    const int64_t out = ((int64_t)b * cap_m + j) * d;
+    gated_block_sum<T>(rowK, rowV, m, d, g, CK + out, CV + out, w);
+    __syncthreads();
+  }
+}
+
+// ---- scratch pad: entries of blocks closed by tree nodes ------------------------------------
+// grid: (D, B, active compressors).  Row v of the scratch pad of compressor m is written either
+// with the block that v's token closes (positions pos_v - m + 1 .. pos_v of prefix + path(v)) or
+// with zeros.
+template <typename T>
+__global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
+                              const T* __restrict__ rawK, const T* __restrict__ rawV,
+                              const int32_t* __restrict__ L, const T* __restrict__ treeK,
+                              const T* __restrict__ treeV, const int32_t* __restrict__ parents,
+                              const float* __restrict__ g4, const float* __restrict__ g128,
+                              T* scrK4, T* scrV4, T* scrK128, T* scrV128, int32_t* status) {
+  __shared__ const T* rowK[128];
+  __shared__ const T* rowV[128];
+  __shared__ float w[128];
+  __shared__ int path[kMaxD];   // path[k] = ancestor of v at depth k
+  __shared__ int s_depth;
+  __shared__ int s_ok;
+  const int v = blockIdx.x;
+  const int b = blockIdx.y;
+  int which = blockIdx.z;  // index among active compressors
+  int m;
+  if ((comp_mask & TV_COMP_C4) && which == 0) {
+    m = 4;
+  } else {
+    m = 128;
+  }
+  const float* g = (m == 4) ? g4 : g128;
+  T* outK = (m == 4) ? scrK4 : scrK128;
+  T* outV = (m == 4) ? scrV4 : scrV128;
+  const int64_t out = ((int64_t)b * D + v) * d;
+  const int Lb = L[b];
+  const int32_t* par = parents + (int64_t)b * D;
+
+  if (threadIdx.x == 0) {
+    int ok = (Lb >= 0 && Lb <= raw_cap) ? 1 : 0;
+    int dep = 0;
+    int u = v;
+    int chain[kMaxD];
+    for (int step = 0; step < D && ok; ++step) {
+      chain[dep] = u;
+      if (u == 0) break;
+      const int p = par[u];
+      if (p < 0 || p >= u) { ok = 0; break; }
+      u = p;
+      ++dep;
+    }
+    if (ok && par[0] != -1) ok = 0;
+    if (ok) {
+      for (int k = 0; k <= dep; ++k) path[k] = chain[dep - k];
+    } else {
+      record_error(status, (Lb < 0 || Lb > raw_cap) ? TV_ERR_CAPACITY : TV_ERR_BAD_TREE);
+    }
+    s_depth = dep;
+    s_ok = ok;
+  }
+  __syncthreads();
+  const int pos = Lb + s_depth;
+  const bool closes = s_ok && ((pos + 1) % m == 0);
+  if (!closes) {
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+      store_f(outK + out + i, 0.f);
+      store_f(outV + out + i, 0.f);
+    }
+    return;
+  }
+  for (int t = threadIdx.x; t < m; t += blockDim.x) {
+    const int p = pos + 1 - m + t;   // >= 0 because pos + 1 is a positive multiple of m
+    if (p < Lb) {
+      const int64_t row = (int64_t)b * raw_cap + p;
+      rowK[t] = rawK + row * d;
+      rowV[t] = rawV + row * d;
+    } else {
+      const int64_t row = (int64_t)b * D + path[p - Lb];
+      rowK[t] = treeK + row * d;
+      rowV[t] = treeV + row * d;
+    }
+  }
+  __syncthreads();
+  gated_block_sum<T>(rowK, rowV, m, d, g, outK + out, outV + out, w);
+}
+
+// ---- refresh: commit the accepted path --------------------------------------------------------
+// One CTA per request.  Copies the accepted tokens' K/V into the raw rows L .. L+n-1, copies the
+// scratch rows of accepted nodes that close a block into the persistent entries, advances L.
+__device__ __forceinline__ void copy_row(void* dst, const void* src, int bytes) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) d4[i] = s4[i];
+}
+
+__global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_cap,
+                               int64_t c4_cap, int64_t c128_cap,
+                               const int32_t* __restrict__ accept_len,
+                               const int32_t* __restrict__ path_all, const char* treeK,
+                               const char* treeV, const char* scrK4, const char* scrV4,
+                               const char* scrK128, const char* scrV128, char* rawK, char* rawV,
+                               char* c4K, char* c4V, char* c128K, char* c128V, int32_t* L,
+                               int32_t* committed, int32_t* status) {
+  __shared__ int s_ok;
+  __shared__ int s_L;
+  __shared__ int s_n;
+  const int b = blockIdx.x;
+  const int64_t row_bytes = (int64_t)d * es;
+  const int32_t* path = path_all + (int64_t)b * D;
+  if (threadIdx.x == 0) {
+    const int Lb = L[b];
+    const int n = accept_len[b];
+    int ok = 1, code = 0;
+    if (n < 1 || n > D || Lb < 0) { ok = 0; code = TV_ERR_ARG; }
+    for (int i = 0; ok && i < n; ++i)
+      if (path[i] < 0 || path[i] >= D) { ok = 0; code = TV_ERR_ARG; }
+    if (ok) {
+      const int64_t Lnew = (int64_t)Lb + n;
+      if (Lnew > raw_cap) { ok = 0; code = TV_ERR_CAPACITY; }
+      if ((comp_mask & TV_COMP_C4) && Lnew / 4 > c4_cap) { ok = 0; code = TV_ERR_CAPACITY; }
+      if ((comp_mask & TV_COMP_C128) && Lnew / 128 > c128_cap) { ok = 0; code = TV_ERR_CAPACITY; }
+    }
+    if (!ok) record_error(status, code);
+    s_ok = ok;
+    s_L = Lb;
+    s_n = n;
+  }
+  __syncthreads();
+  int32_t* cpos = committed + (int64_t)b * D;
+  if (!s_ok) {
+    for (int i = threadIdx.x; i < D; i += blockDim.x) cpos[i] = -1;
+    return;
+  }
+  const int Lb = s_L, n = s_n;
+  for (int i = 0; i < n; ++i) {
+    const int64_t src = ((int64_t)b * D + path[i]) * row_bytes;
+    const int64_t dst = ((int64_t)b * raw_cap + Lb + i) * row_bytes;
+    copy_row(rawK + dst, treeK + src, (int)row_bytes);
+    copy_row(rawV + dst, treeV + src, (int)row_bytes);
+  }
+  for (int e = Lb; e < Lb + n; ++e) {
+    const int u = path[e - Lb];
+    const int64_t src = ((int64_t)b * D + u) * row_bytes;
+    if ((comp_mask & TV_COMP_C4) && ((e + 1) & 3) == 0) {
+      const int64_t dst = ((int64_t)b * c4_cap + (e + 1) / 4 - 1) * row_bytes;
+      copy_row(c4K + dst, scrK4 + src, (int)row_bytes);
+      copy_row(c4V + dst, scrV4 + src, (int)row_bytes);
+    }
+    if ((comp_mask & TV_COMP_C128) && ((e + 1) & 127) == 0) {
+      const int64_t dst = ((int64_t)b * c128_cap + (e + 1) / 128 - 1) * row_bytes;
+      copy_row(c128K + dst, scrK128 + src, (int)row_bytes);
+      copy_row(c128V + dst, scrV128 + src, (int)row_bytes);
+    }
+  }
+  for (int i = threadIdx.x; i < D; i += blockDim.x) cpos[i] = i < n ? Lb + i : -1;
+  __syncthreads();
+  if (threadIdx.x == 0) L[b] = Lb + n;
+}
+
+}  // namespace tv
+
+// ---- launchers --------------------------------------------------------------------------------
+template <typename T>
+static int launch_prefill_t(const tv_shape* s, const void* rawK, const void* rawV,
+                            const int32_t* L, const float* g4, const float* g128, void* c4K,
+                            void* c4V, void* c128K, void* c128V, int32_t* status,
+                            cudaStream_t stream) {
+  const int d = s->d;
+  if (s->comp_mask & TV_COMP_C4) {
+    const int64_t cap = s->c4_cap;
+    const unsigned gx = (unsigned)(cap < 1 ? 1 : (cap > (1 << 20) ? (1 << 20) : cap));
+    tv::prefill_kernel<T><<<dim3(gx, s->B), tv::kCompressThreads, 0, stream>>>(
+        4, d, s->raw_cap, cap, (const T*)rawK, (const T*)rawV, L, g4, (T*)c4K, (T*)c4V, status);
+    if (int rc = tv_check_launch("tv_prefill_compress (C4)")) return rc;
+  }
+  if (s->comp_mask & TV_COMP_C128) {
+    const int64_t cap = s->c128_cap;
+    const unsigned gx = (unsigned)(cap < 1 ? 1 : (cap > (1 << 20) ? (1 << 20) : cap));
+    tv::prefill_kernel<T><<<dim3(gx, s->B), tv::kCompressThreads, 0, stream>>>(
+        128, d, s->raw_cap, cap, (const T*)rawK, (const T*)rawV, L, g128, (T*)c128K,
+        (T*)c128V, status);
+    if (int rc = tv_check_launch("tv_prefill_compress (C128)")) return rc;
+  }
+  return TV_OK;
+}
+
+int tv_launch_prefill(const tv_shape* s, const void* rawK, const void* rawV, const int32_t* L,
+                      const float* g4, const float* g128, void* c4K, void* c4V, void* c128K,
+                      void* c128V, int32_t* status, cudaStream_t stream) {
+  if (s->dtype == TV_BF16)
+    return launch_prefill_t<__nv_bfloat16>(s, rawK, rawV, L, g4, g128, c4K, c4V, c128K, c128V,
+                                           status, stream);
+  return launch_prefill_t<float>(s, rawK, rawV, L, g4, g128, c4K, c4V, c128K, c128V, status,
+                                 stream);
+}
+
+int tv_launch_branch(const tv_shape* s, const void* rawK, const void* rawV, const int32_t* L,
+                     const void* treeK, const void* treeV, const int32_t* parents,
+                     const float* g4, const float* g128, void* scrK4, void* scrV4,
+                     void* scrK128, void* scrV128, int32_t* status, cudaStream_t stream) {
+  const int n_comp = ((s->comp_mask & TV_COMP_C4) ? 1 : 0) + ((s->comp_mask & TV_COMP_C128) ? 1 : 0);
+  const dim3 grid(s->D, s->B, n_comp);
+  if (s->dtype == TV_BF16) {
+    using T = __nv_bfloat16;
+    tv::branch_kernel<T><<<grid, tv::kCompressThreads, 0, stream>>>(
+        s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
+        (const T*)treeK, (const T*)treeV, parents, g4, g128, (T*)scrK4, (T*)scrV4,
+        (T*)scrK128, (T*)scrV128, status);
+  } else {
+    using T = float;
+    tv::branch_kernel<T><<<grid, tv::kCompressThreads, 0, stream>>>(
+        s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
+        (const T*)treeK, (const T*)treeV, parents, g4, g128, (T*)scrK4, (T*)scrV4,
+        (T*)scrK128, (T*)scrV128, status);
+  }
+  return tv_check_launch("tv_branch_compress");
+}
+
+int tv_launch_refresh(const tv_shape* s, const int32_t* accept_len, const int32_t* path,
+                      const void* treeK, const void* treeV, const void* scrK4, const void* scrV4,
+                      const void* scrK128, const void* scrV128, void* rawK, void* rawV,
+                      void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
+                      int32_t* committed, int32_t* status, cudaStream_t stream) {
+  const int es = s->dtype == TV_BF16 ? 2 : 4;
+  tv::refresh_kernel<<<s->B, 128, 0, stream>>>(
+      s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap, accept_len, path,
+      (const char*)treeK, (const char*)treeV, (const char*)scrK4, (const char*)scrV4,
+      (const char*)scrK128, (const char*)scrV128, (char*)rawK, (char*)rawV, (char*)c4K,
+      (char*)c4V, (char*)c128K, (char*)c128V, L, committed, status);
+  return tv_check_launch("tv_refresh_commit");
+}

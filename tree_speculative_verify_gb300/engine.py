@@ -1,0 +1,162 @@
+"""Device buffers and the five-call verify round (allocation and marshalling only).
+
+``DeviceState`` holds one batch's persistent cache (raw K/V, C4 and C128 entries, committed
+lengths); ``RoundBuffers`` holds one round's inputs (tree, tokens, queries, tree K/V), the plan,
+the scratch pad and the outputs.  ``verify_round`` enqueues tv_build_ancestor_mask,
+tv_branch_compress, tv_tree_verify_attn, tv_accept_walk and tv_refresh_commit on one stream with
+no host synchronisation, as "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for
+Efficient Inference" §4.1/§4.4 describe one target-verify stage.  Every step runs in the CUDA
+library; PyTorch only allocates memory.
+"""
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+
+def shape_for(wl, attn_kernel=_lib.TV_ATTN_AUTO, B=None):
+    comp = 0
+    if 4 in wl.ms:
+        comp |= _lib.TV_COMP_C4
+    if 128 in wl.ms:
+        comp |= _lib.TV_COMP_C128
+    return _lib.make_shape(
+        B=wl.B if B is None else B, D=wl.D, H=wl.H, d=wl.d, W=wl.W,
+        tail_mode=_lib.TV_TAIL_WINDOW if wl.tail_mode == "window" else _lib.TV_TAIL_REMAINDER,
+        comp_mask=comp, dtype=_lib.TV_F32 if wl.dtype == "f32" else _lib.TV_BF16,
+        n_sel=wl.n_sel, attn_kernel=attn_kernel, raw_cap=wl.raw_cap,
+        c4_cap=wl.cap4 if 4 in wl.ms else 0, c128_cap=wl.cap128 if 128 in wl.ms else 0)
+
+
+@dataclass
+class DeviceState:
+    rawK: torch.Tensor
+    rawV: torch.Tensor
+    c4K: torch.Tensor
+    c4V: torch.Tensor
+    c128K: torch.Tensor
+    c128V: torch.Tensor
+    L: torch.Tensor
+
+    def clone(self):
+        return DeviceState(*(t.clone() for t in (self.rawK, self.rawV, self.c4K, self.c4V,
+                                                 self.c128K, self.c128V, self.L)))
+
+
+@dataclass
+class RoundBuffers:
+    parents: torch.Tensor
+    draft: torch.Tensor
+    target: torch.Tensor
+    Q: torch.Tensor
+    treeK: torch.Tensor
+    treeV: torch.Tensor
+    sel: torch.Tensor
+    g4: torch.Tensor
+    g128: torch.Tensor
+    anc: torch.Tensor
+    depth: torch.Tensor
+    raw_lo: torch.Tensor
+    vis4: torch.Tensor
+    vis128: torch.Tensor
+    scrK4: torch.Tensor
+    scrV4: torch.Tensor
+    scrK128: torch.Tensor
+    scrV128: torch.Tensor
+    O: torch.Tensor
+    lse: torch.Tensor
+    accept_len: torch.Tensor
+    path: torch.Tensor
+    bonus: torch.Tensor
+    committed: torch.Tensor
+    status: torch.Tensor
+    workspace: torch.Tensor
+
+
+def alloc_state(wl, device="cuda"):
+    """Persistent cache of the workload on the device: raw rows uploaded, compressed rows zero."""
+    dt = wl.torch_dtype
+    z = lambda n: torch.zeros((wl.B, max(n, 1), wl.d), dtype=dt, device=device)
+    return DeviceState(
+        rawK=wl.rawK.to(device), rawV=wl.rawV.to(device),
+        c4K=z(wl.cap4 if 4 in wl.ms else 0), c4V=z(wl.cap4 if 4 in wl.ms else 0),
+        c128K=z(wl.cap128 if 128 in wl.ms else 0), c128V=z(wl.cap128 if 128 in wl.ms else 0),
+        L=torch.as_tensor(wl.L, dtype=torch.int32).to(device))
+
+
+def alloc_round(wl, shape, device="cuda"):
+    dt = wl.torch_dtype
+    B, D, H, d = wl.B, wl.D, wl.H, wl.d
+    i32 = dict(dtype=torch.int32, device=device)
+    i64 = dict(dtype=torch.int64, device=device)
+    ws = _lib.tv_workspace_size(shape)
+    g4 = wl.g[4].to(device) if 4 in wl.g else torch.zeros(d, device=device)
+    g128 = wl.g[128].to(device) if 128 in wl.g else torch.zeros(d, device=device)
+    sel = torch.as_tensor(wl.sel, dtype=torch.int32).to(device) if wl.sel is not None else None
+    return RoundBuffers(
+        parents=torch.as_tensor(wl.parents, dtype=torch.int32).to(device),
+        draft=torch.as_tensor(wl.draft, dtype=torch.int32).to(device),
+        target=torch.as_tensor(wl.target, dtype=torch.int32).to(device),
+        Q=wl.Q.to(device), treeK=wl.treeK.to(device), treeV=wl.treeV.to(device), sel=sel,
+        g4=g4, g128=g128,
+        anc=torch.zeros((B, D), **i64), depth=torch.zeros((B, D), **i32),
+        raw_lo=torch.zeros((B, D), **i32), vis4=torch.zeros((B, D), **i64),
+        vis128=torch.zeros((B, D), **i64),
+        scrK4=torch.zeros((B, D, d), dtype=dt, device=device),
+        scrV4=torch.zeros((B, D, d), dtype=dt, device=device),
+        scrK128=torch.zeros((B, D, d), dtype=dt, device=device),
+        scrV128=torch.zeros((B, D, d), dtype=dt, device=device),
+        O=torch.zeros((B, D, H, d), dtype=dt, device=device),
+        lse=torch.zeros((B, D, H), dtype=torch.float32, device=device),
+        accept_len=torch.zeros(B, **i32), path=torch.zeros((B, D), **i32),
+        bonus=torch.zeros(B, **i32), committed=torch.zeros((B, D), **i32),
+        status=torch.zeros(1, **i32),
+        workspace=torch.empty(max(ws, 256), dtype=torch.uint8, device=device))
+
+
+def prefill(shape, st, rb, stream=None):
+    _lib.tv_prefill_compress(shape, st.rawK, st.rawV, st.L, rb.g4, rb.g128, st.c4K, st.c4V,
+                             st.c128K, st.c128V, rb.status, stream)
+
+
+def plan(shape, st, rb, stream=None):
+    _lib.tv_build_ancestor_mask(shape, rb.parents, st.L, rb.anc, rb.depth, rb.raw_lo, rb.vis4,
+                                rb.vis128, rb.status, stream)
+
+
+def branch_compress(shape, st, rb, stream=None):
+    _lib.tv_branch_compress(shape, st.rawK, st.rawV, st.L, rb.treeK, rb.treeV, rb.parents, rb.g4,
+                            rb.g128, rb.scrK4, rb.scrV4, rb.scrK128, rb.scrV128, rb.status, stream)
+
+
+def attention(shape, st, rb, scale=None, stream=None):
+    if scale is None:
+        scale = 1.0 / math.sqrt(shape.d)
+    _lib.tv_tree_verify_attn(shape, rb.Q, st.c4K, st.c4V, rb.sel, st.c128K, st.c128V, st.rawK,
+                             st.rawV, st.L, rb.treeK, rb.treeV, rb.anc, rb.raw_lo, rb.vis4,
+                             rb.vis128, rb.scrK4, rb.scrV4, rb.scrK128, rb.scrV128, scale, rb.O,
+                             rb.lse, rb.workspace, rb.status, stream)
+
+
+def accept(shape, st, rb, stream=None):
+    _lib.tv_accept_walk(shape, rb.parents, rb.draft, rb.target, rb.accept_len, rb.path, rb.bonus,
+                        rb.status, stream)
+
+
+def refresh(shape, st, rb, stream=None):
+    _lib.tv_refresh_commit(shape, rb.accept_len, rb.path, rb.treeK, rb.treeV, rb.scrK4, rb.scrV4,
+                           rb.scrK128, rb.scrV128, st.rawK, st.rawV, st.c4K, st.c4V, st.c128K,
+                           st.c128V, st.L, rb.committed, rb.status, stream)
+
+
+def verify_round(shape, st, rb, scale=None, stream=None, commit=True):
+    """One target-verify round: plan, scratch pad, attention, acceptance, refresh."""
+    plan(shape, st, rb, stream)
+    branch_compress(shape, st, rb, stream)
+    attention(shape, st, rb, scale, stream)
+    accept(shape, st, rb, stream)
+    if commit:
+        refresh(shape, st, rb, stream)
