@@ -36,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-N_SETS = 3   # rotating copies of the state: each step touches data last used 3 steps earlier
+
 WORKLOAD_DESC = {
     "serving": "serving batch: B=64, L~U{1024..8192}, D=8 (top-2 tree, 4 steps), H=64x1, d=512, "
                "C4+C128+W128, bf16",
@@ -56,14 +56,18 @@ def parse():
     ap.add_argument("--workload", choices=list(WORKLOAD_DESC), default="serving")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-kernel", choices=["auto", "simt", "tcgen05"], default="auto")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests per GPU (default: the workload's own batch)")
+    ap.add_argument("--sets", type=int, default=3,
+                    help="rotating state copies (3 keeps every step's inputs out of L2)")
     return ap.parse_args()
 
 
-def make_workload(name, rank):
+def make_workload(name, rank, batch=None):
     from tree_speculative_verify_gb300 import workloads
     seed = rank
     if name == "serving":
-        return workloads.serving(seed=seed)
+        return workloads.serving(seed=seed, B=batch or 64)
     if name == "small":
         return workloads.small(seed=seed)
     if name == "long":
@@ -343,11 +347,12 @@ def run_ours(args, world, rank, local):
     tvbuild.build()
     kernel = {"auto": _lib.TV_ATTN_AUTO, "simt": _lib.TV_ATTN_SIMT,
               "tcgen05": _lib.TV_ATTN_TCGEN05}[args.attn_kernel]
-    wl = make_workload(args.workload, rank)
+    wl = make_workload(args.workload, rank, args.batch)
+    n_sets = max(1, args.sets)
     shape = engine.shape_for(wl, kernel)
     stream = torch.cuda.current_stream()
     sets = []
-    for _ in range(N_SETS):
+    for _ in range(n_sets):
         st = engine.alloc_state(wl)
         rb = engine.alloc_round(wl, shape)
         engine.prefill(shape, st, rb, stream)
@@ -360,7 +365,7 @@ def run_ours(args, world, rank, local):
           for _ in range(args.steps)]
 
     def step(i, timed=None):
-        st, rb, L0 = sets[i % N_SETS]
+        st, rb, L0 = sets[i % n_sets]
         st.L.copy_(L0, non_blocking=True)
         engine.plan(shape, st, rb, stream)
         engine.branch_compress(shape, st, rb, stream)
@@ -407,7 +412,7 @@ def run_ours(args, world, rank, local):
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
     def e2e_step(i):
-        s_, r_, l_ = sets[i % N_SETS]
+        s_, r_, l_ = sets[i % n_sets]
         s_.L.copy_(l_, non_blocking=True)
         for dst, src in zip([r_.Q, r_.treeK, r_.treeV, r_.parents, r_.draft, r_.target], host_in):
             dst.copy_(src, non_blocking=True)
@@ -445,7 +450,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.workload], "B_per_gpu": wl.B, "D": wl.D,
                    "H": wl.H, "d": wl.d, "attention_kernel": tc_name,
-                   "l2": f"inputs larger than L2: {N_SETS} rotating state copies, "
+                   "l2": f"inputs larger than L2: {n_sets} rotating state copies, "
                          f"{kv_bytes / 1e6:.0f} MB KV per step each",
                    "parallelism": f"replicas x{world} (requests sharded, no collective)"},
         "roofline": {"bound": "tensor", "achieved": tflops,

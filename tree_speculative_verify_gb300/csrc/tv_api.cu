@@ -136,12 +136,12 @@ static SimtPlan simt_plan(const tv_shape* s) {
   chunk = (chunk + 7) / 8 * 8;
   p.n_chunks = (int)n_chunks;
   p.chunk = (int)chunk;
-  p.part_bytes = (size_t)s->B * DH * n_chunks * (s->d + 2) * sizeof(float);
+  p.part_bytes = (size_t)s->B * DH * n_chunks * (s->d + 4) * sizeof(float);
   return p;
 }
 
 static bool tc_supported(const tv_shape* s) {
-  return s->dtype == TV_BF16 && s->d == 512 && tv_tc_available();
+  return tv_tc_shape_ok(s) && tv_tc_available();
 }
 
 static bool use_tc(const tv_shape* s) {
@@ -162,8 +162,8 @@ extern "C" int tv_attn_kernel_for(const tv_shape* s) {
   if (int rc = check_shape(s, "tv_attn_kernel_for")) return rc;
   if (!use_tc(s)) return TV_ATTN_SIMT;
   if (!tc_supported(s))
-    return tv_set_error(TV_ERR_DTYPE, "tv_attn_kernel_for: the tcgen05 kernel needs bf16, d = 512 "
-                        "and an sm_103 device");
+    return tv_set_error(TV_ERR_DTYPE, "tv_attn_kernel_for: the tcgen05 kernel needs bf16, d = 512, D <= 8, "
+                        "n_sel = 0 and an sm_103 device");
   return TV_ATTN_TCGEN05;
 }
 
@@ -343,7 +343,7 @@ extern "C" int tv_tree_verify_attn(const tv_shape* s, const void* Q, const void*
   if (use_tc(s)) {
     if (!tc_supported(s))
       return tv_set_error(TV_ERR_DTYPE,
-                          "%s: the tcgen05 kernel needs bf16, d = 512 and an sm_103 device", fn);
+                          "%s: the tcgen05 kernel needs bf16, d = 512, D <= 8, n_sel = 0 and an sm_103 device", fn);
     auto p = make_params<__nv_bfloat16>(s, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L, treeK,
                                         treeV, anc, raw_lo, scr_vis4, scr_vis128, scrK4, scrV4,
                                         scrK128, scrV128, scale, O, lse, status);

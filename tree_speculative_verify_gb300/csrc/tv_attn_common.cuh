@@ -41,7 +41,7 @@ struct AttnParams {
   float scale_log2;   // logit scale times log2(e)
   int n_chunks;       // split-KV chunks per request
   int chunk;          // entries per chunk
-  float* part;        // [B][D*H][n_chunks][d + 2] partial (o[d], m, l)
+  float* part;        // [B][D*H][n_chunks][d + 4] partial (o[d], m, l, 2 pad)
   T* O;
   float* lse;
   int32_t* status;
@@ -202,22 +202,22 @@ __global__ void merge_kernel(int rows, int d, int n_chunks, const float* __restr
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const float* pr = part + (int64_t)row * n_chunks * (d + 2);
+  const float* pr = part + (int64_t)row * n_chunks * (d + 4);
   float M = -INFINITY;
   for (int c = 0; c < n_chunks; ++c) {
-    const float* pc = pr + (int64_t)c * (d + 2);
+    const float* pc = pr + (int64_t)c * (d + 4);
     if (pc[d + 1] > 0.f) M = fmaxf(M, pc[d]);
   }
   float denom = 0.f;
   for (int c = 0; c < n_chunks; ++c) {
-    const float* pc = pr + (int64_t)c * (d + 2);
+    const float* pc = pr + (int64_t)c * (d + 4);
     if (pc[d + 1] > 0.f) denom += exp2f(pc[d] - M) * pc[d + 1];
   }
   const float inv = denom > 0.f ? 1.f / denom : 0.f;
   for (int i = lane; i < d; i += 32) {
     float acc = 0.f;
     for (int c = 0; c < n_chunks; ++c) {
-      const float* pc = pr + (int64_t)c * (d + 2);
+      const float* pc = pr + (int64_t)c * (d + 4);
       if (pc[d + 1] > 0.f) acc += exp2f(pc[d] - M) * pc[i];
     }
     store_f(O + (int64_t)row * d + i, acc * inv);

@@ -119,7 +119,7 @@ simt_attn_kernel(AttnParams<T> p) {
     m_run = m_new;
   }
   if (!row_ok) return;
-  float* part = p.part + (((int64_t)b * DH + row) * p.n_chunks + c) * (d + 2);
+  float* part = p.part + (((int64_t)b * DH + row) * p.n_chunks + c) * (d + 4);
 #pragma unroll
   for (int k = 0; k < kMaxHeadDim / 32; ++k)
     if (k < per_lane) part[lane + 32 * k] = o[k];
