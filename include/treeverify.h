@@ -197,6 +197,29 @@ int tv_tree_verify_attn(const tv_shape* shape, const void* Q, const void* c4K, c
                         tv_stream_t stream);
 
 /*
+ * tv_tree_verify_attn without a workspace argument, for callers that cannot allocate device
+ * memory (an engine that reserved all free memory for its own page pool, a decode loop that must
+ * not pay cudaMalloc's implicit synchronisation, a plug-in host without an allocator).  The report
+ * has no counterpart: this is a convenience of the library.  Same arguments, semantics and
+ * outputs as tv_tree_verify_attn, minus workspace / ws_bytes.  The split-KV partial results live
+ * in a 32 MiB array inside the library image, held by every GPU that loads the library until the
+ * process exits; a shape whose tv_workspace_size exceeds it is rejected with TV_ERR_WORKSPACE.
+ * The first call on a device resolves the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls share the array:
+ * calls that overlap on the GPU race on it (its previous contents are never read, nothing needs
+ * clearing).  It allocates nothing, neither on the device nor through any library.
+ */
+int tv_tree_verify_attn_noalloc(const tv_shape* shape, const void* Q, const void* c4K,
+                                const void* c4V, const int32_t* sel, const void* c128K,
+                                const void* c128V, const void* rawK, const void* rawV,
+                                const int32_t* L, const void* treeK, const void* treeV,
+                                const uint64_t* anc, const int32_t* raw_lo,
+                                const uint64_t* scr_vis4, const uint64_t* scr_vis128,
+                                const void* scrK4, const void* scrV4, const void* scrK128,
+                                const void* scrV128, float scale, void* O, float* lse,
+                                int32_t* status, tv_stream_t stream);
+
+/*
  * Accepted-path selection ([TSD-V4] §3.2, §4.1): greedy walk from the root; at each node take
  * the lowest-numbered child whose draft token equals the node's target token; stop when none.
  *   parents, draft, target [B][D] int32 in

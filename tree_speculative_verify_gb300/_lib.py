@@ -30,7 +30,7 @@ EXPORTS = (
     "tv_version", "tv_status_string", "tv_last_error_string", "tv_workspace_size",
     "tv_attn_kernel_for",
     "tv_build_ancestor_mask", "tv_prefill_compress", "tv_branch_compress",
-    "tv_tree_verify_attn", "tv_accept_walk", "tv_refresh_commit",
+    "tv_tree_verify_attn", "tv_accept_walk", "tv_refresh_commit", "tv_tree_verify_attn_noalloc",
 )
 
 
@@ -66,6 +66,8 @@ _SIGS = {
     "tv_branch_compress": ([_SHAPE] + [_P] * 13 + [_P], ctypes.c_int),
     "tv_tree_verify_attn": ([_SHAPE] + [_P] * 19 + [ctypes.c_float, _P, _P, _P, ctypes.c_size_t,
                                                     _P, _P], ctypes.c_int),
+    "tv_tree_verify_attn_noalloc": ([_SHAPE] + [_P] * 19 + [ctypes.c_float, _P, _P, _P, _P],
+                                    ctypes.c_int),
     "tv_accept_walk": ([_SHAPE] + [_P] * 7 + [_P], ctypes.c_int),
     "tv_refresh_commit": ([_SHAPE] + [_P] * 17 + [_P], ctypes.c_int),
 }
@@ -169,6 +171,19 @@ def tv_tree_verify_attn(shape, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L, tr
                                     ctypes.c_float(scale), _p(O), _p(lse), _p(workspace),
                                     ctypes.c_size_t(ws_bytes), _p(status), _stream(stream))
     _check("tv_tree_verify_attn", rc)
+
+
+def tv_tree_verify_attn_noalloc(shape, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L, treeK,
+                                treeV, anc, raw_lo, scr_vis4, scr_vis128, scrK4, scrV4, scrK128,
+                                scrV128, scale, O, lse, status, stream=None):
+    """tv_tree_verify_attn for callers that cannot allocate: no workspace argument; the library's
+    built-in scratch holds the split-KV partials (see include/treeverify.h)."""
+    rc = load().tv_tree_verify_attn_noalloc(
+        ctypes.byref(shape), _p(Q), _p(c4K), _p(c4V), _p(sel), _p(c128K), _p(c128V), _p(rawK),
+        _p(rawV), _p(L), _p(treeK), _p(treeV), _p(anc), _p(raw_lo), _p(scr_vis4), _p(scr_vis128),
+        _p(scrK4), _p(scrV4), _p(scrK128), _p(scrV128), ctypes.c_float(scale), _p(O), _p(lse),
+        _p(status), _stream(stream))
+    _check("tv_tree_verify_attn_noalloc", rc)
 
 
 def tv_accept_walk(shape, parents, draft, target, accept_len, path, bonus, status, stream=None):
