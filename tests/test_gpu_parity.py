@@ -150,3 +150,34 @@ def test_two_rounds_in_a_row():
     engine.verify_round(shape, st, rb2)
     torch.cuda.synchronize()
     check_round(wl2, res2, st_before, st, rb2, range(wl.B))
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "serving_reduced", "c128_boundary"])
+def test_prefill_compress_matches_oracle(name):
+    """tv_prefill_compress writes every complete C4 / C128 block of the committed prefix."""
+    from helpers import TOL, close, np32
+    if name == "tiny":
+        wl = workloads.tiny(L=255)
+    elif name == "small":
+        wl = workloads.small()
+    elif name == "serving_reduced":
+        wl = workloads.serving(B=5, L=(1000, 3000))
+    else:
+        wl = _edge("c128b", L=(255, 640), B=4)
+    from tree_speculative_verify_gb300 import engine
+    shape = engine.shape_for(wl)
+    st = engine.alloc_state(wl)
+    rb = engine.alloc_round(wl, shape)
+    engine.prefill(shape, st, rb)
+    torch.cuda.synchronize()
+    assert int(rb.status.item()) == 0
+    comp = oracle_prefix(wl)
+    tol = TOL[wl.dtype]
+    for m in wl.ms:
+        gk = np32(st.c4K if m == 4 else st.c128K)
+        gv = np32(st.c4V if m == 4 else st.c128V)
+        for b in range(wl.B):
+            n = int(wl.L[b]) // m
+            close(gk[b, :n], comp[m][0][b, :n], tol, f"prefill C{m} K request {b}")
+            close(gv[b, :n], comp[m][1][b, :n], tol, f"prefill C{m} V request {b}")
+            assert np.all(gk[b, n:] == 0)      # nothing written beyond the valid entries

@@ -52,7 +52,8 @@ namespace tc {
 
 using namespace sm100;
 
-constexpr int kThreads = 320;          // producer, MMA issuer, 8 softmax warps
+constexpr int kSmxWarps = 8;           // softmax warps: 4 (a thread per row) or 8 (two per row)
+constexpr int kThreads = 64 + 32 * kSmxWarps;   // producer, MMA issuer, softmax warps
 constexpr int kSlots = 6;
 constexpr int kSlotBytes = 16384;
 constexpr int kQBytes = 8 * 16384;
@@ -78,7 +79,8 @@ struct Params {
   float scale_log2;
   __nv_bfloat16* O;
   float* lse;
-  float* part;
+  float* part;          // split-KV partials (n_chunks > 1)
+  const int32_t* order; // requests by decreasing tile count (longest first)
   int32_t* status;
 };
 
@@ -136,6 +138,21 @@ __device__ __forceinline__ Tile tile_of(const Layout& y, int t) {
   return x;
 }
 
+// Longest-processing-time-first order of the requests: the pair scheduler starts the longest
+// requests first, so the last wave holds the shortest work items.  rank(b) = number of requests
+// with more tiles, ties broken by index; order[rank(b)] = b.
+__global__ void order_kernel(Params p, int32_t* order) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  const int tb = layout_of(p, b).T;
+  int rank = 0;
+  for (int j = 0; j < p.B; ++j) {
+    const int tj = layout_of(p, j).T;
+    rank += (tj > tb || (tj == tb && j < b)) ? 1 : 0;
+  }
+  order[rank] = b;
+}
+
 struct __align__(1024) Smem {
   uint8_t q[kQBytes];
   uint8_t ring[kSlots][kSlotBytes];
@@ -143,7 +160,7 @@ struct __align__(1024) Smem {
   uint64_t empty[kSlots];      // the pair's MMAs are done with the slot
   uint64_t q_full;
   uint64_t s_full[2];
-  uint64_t p_full[2];          // (leader) P written by all 16 softmax warps of the pair
+  uint64_t p_full[2];          // (leader) P written by both CTAs' softmax warps
   uint64_t pv_done;
   uint64_t o_full;
   uint64_t drain;
@@ -365,20 +382,28 @@ __device__ void mma_issuer(const Params& p, Smem& sm, const Layout& y, int tb, i
   mbar_wait(&sm.drain, 0, &never, kTimeoutNs / 4);
 }
 
-// ---- softmax / epilogue (warps 2..9 of both CTAs) -------------------------------------------
-// Two warps per TMEM lane quadrant: warp w (2..9) serves rows 32*(w%4) .. +31 and the column half
-// ch = (w-2)/4 of every S tile (64 of 128 entries) and of this CTA's O (128 of 256 columns).
-// The two threads of a row exchange their partial row maxima through shared memory once per tile,
-// so both apply the same running maximum; their partial row sums are combined at the end.
+// ---- softmax / epilogue (softmax warps of both CTAs) ----------------------------------------
+// kSmxWarps warps; warp w (>= 2) serves TMEM lane quadrant w % 4 (rows 32*(w%4) .. +31).  With 8
+// warps, two threads share a row (column half ch = (w-2)/4 each) and exchange their partial row
+// maxima through shared memory once per tile; with 4 warps one thread owns the whole row.  Both
+// threads of a row apply the same running maximum; partial row sums are combined at the end.
+constexpr int kCh = kSmxWarps / 4;          // threads per row
+constexpr int kColsPerThread = 128 / kCh;   // S columns per thread and tile
+constexpr int kOColsPerThread = 256 / kCh;  // O columns per thread
+
 __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+}
+// all softmax warps of this CTA
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 5, %0;" ::"n"(kSmxWarps * 32) : "memory");
 }
 
 __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int half, int chunk,
                                  const Layout& y, int tb, int te) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
-  const int ch = (warp - 2) >> 2;
+  const int ch = (warp - 2) >> 2;           // always 0 with 4 softmax warps
   const int row = 32 * quad + lane;
   const int grow = 128 * rt + row;
   const bool row_ok = grow < p.DH;
@@ -414,8 +439,7 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
   for (int i = 0; i < n && ok; ++i) {
     const Tile x = tile_of(y, tb + i);
     const int sb = i & 1;
-    const int c0 = 64 * ch;                 // first S column of this thread
-    const bool has_cols = c0 < x.nqk;      // warp-uniform
+    const int c0 = kColsPerThread * ch;     // first S column of this thread
     // the wait result is made warp-uniform: tcgen05.ld below is warp-collective
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs))) {
       fail(sm, p.status);
@@ -423,12 +447,14 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
       break;
     }
     tc_fence_after();
-    float s[64];
-    if (has_cols) {
+    float s[kColsPerThread];
+    {
       uint32_t* sr = reinterpret_cast<uint32_t*>(s);
-      tmem_ld32(tmem + lane_base + 128 * sb + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      if (c0 + 32 < x.nqk)
-        tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+#pragma unroll
+      for (int c = 0; c < kColsPerThread / 32; ++c)
+        if (c0 + 32 * c < x.nqk)
+          tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32 * c,
+                    *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
       tmem_wait_ld();
     }
     // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
@@ -438,10 +464,10 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
     const bool full_tile = (x.kind == kC4 || x.kind == kC128) && x.valid >= 128;
     if (full_tile) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+      for (int j = 0; j < kColsPerThread; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
     } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      for (int j = 0; j < kColsPerThread; ++j) {
         const int col = c0 + j;
         bool vis = col < x.valid;
         if (x.kind == kRaw) vis = vis && (x.row0 + col >= raw_lo);
@@ -450,11 +476,13 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
         mx[j & 7] = fmaxf(mx[j & 7], s[j]);
       }
     }
-    const float mine = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-    sm.xmax[sb][ch][row] = mine;
-    pair_sync(quad);
-    const float raw_max = fmaxf(mine, sm.xmax[sb][ch ^ 1][row]);
+    float raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    if (kCh == 2) {
+      sm.xmax[sb][ch][row] = raw_max;
+      pair_sync(quad);
+      raw_max = fmaxf(raw_max, sm.xmax[sb][ch ^ 1][row]);
+    }
     const float mt = raw_max * sl2;
     const bool grow_max = mt > m_ref + kRescaleThreshold;
     const float m_new = grow_max ? mt : m_ref;
@@ -468,9 +496,9 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
         break;
       }
       tc_fence_after();
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kOColsPerThread / 32; ++c) {
         uint32_t r[32];
-        const uint32_t col = tmem + lane_base + 256 + 128 * ch + 32 * c;
+        const uint32_t col = tmem + lane_base + 256 + kOColsPerThread * ch + 32 * c;
         tmem_ld32(col, r);
         tmem_wait_ld();
 #pragma unroll
@@ -483,24 +511,28 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
     float sum[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) sum[k] = 0.f;
-    uint32_t pk[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg_m));
-      const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg_m));
-      sum[j & 7] += p0 + p1;
-      const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-      pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int c = 0; c < kColsPerThread / 64; ++c) {
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p0 = ex2_approx(fmaf(s[64 * c + 2 * j], sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(s[64 * c + 2 * j + 1], sl2, neg_m));
+        sum[j & 7] += p0 + p1;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      // P column k holds entries 2k and 2k+1
+      if (c0 + 64 * c < x.nqk) tmem_st32(tmem + lane_base + 128 * sb + (c0 >> 1) + 32 * c, pk);
     }
-    if (has_cols) tmem_st32(tmem + lane_base + 128 * sb + 32 * ch, pk);
     const float tsum =
         ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-    l_run = l_run * alpha + (has_cols ? tsum : 0.f);
+    l_run = l_run * alpha + tsum;
     m_ref = m_new;
     tmem_wait_st();
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(p_full_leader[sb]);   // the leader's MMA consumes P
+    softmax_sync();   // one release-arrive per CTA: P of all 128 rows is in TMEM
+    if (warp == 2 && lane == 0) mbar_arrive_cluster(p_full_leader[sb]);
   }
   if (ok && n > 0) {
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, 0, &sm.abort, kTimeoutNs))) {
@@ -508,22 +540,25 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
       ok = false;
     }
   }
-  // combine the two partial row sums (both threads of a row share m_ref); once o_full has been
-  // observed every copy and MMA of this CTA's ring is done, so its first slot holds the exchange
-  float* xsum = reinterpret_cast<float*>(sm.ring[0]);
-  xsum[128 * ch + row] = l_run;
-  pair_sync(quad);
-  const float l_tot = l_run + xsum[128 * (ch ^ 1) + row];
+  float l_tot = l_run;
+  if (kCh == 2) {
+    // combine the two partial row sums (both threads of a row share m_ref); once o_full has been
+    // observed every copy and MMA of this CTA's ring is done, so its first slot holds the exchange
+    float* xsum = reinterpret_cast<float*>(sm.ring[0]);
+    xsum[128 * ch + row] = l_run;
+    pair_sync(quad);
+    l_tot = l_run + xsum[128 * (ch ^ 1) + row];
+  }
   if (!ok) return;
   tc_fence_after();
   const int d = 512;
-  const int ocol = 256 * half + 128 * ch;   // first O column of this thread
+  const int ocol = 256 * half + kOColsPerThread * ch;   // first O column of this thread
   if (p.n_chunks == 1) {
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
     __nv_bfloat16* orow = p.O + ((int64_t)b * p.DH + grow) * d + ocol;
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kOColsPerThread / 32; ++c) {
       uint32_t r[32];
-      tmem_ld32(tmem + lane_base + 256 + 128 * ch + 32 * c, r);
+      tmem_ld32(tmem + lane_base + 256 + kOColsPerThread * ch + 32 * c, r);
       tmem_wait_ld();
       if (row_ok) {
         uint4 w[4];
@@ -544,10 +579,10 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
           l_tot > 0.f ? (m_ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
   } else {
     float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + chunk) * (d + 4);
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kOColsPerThread / 32; ++c) {
       uint32_t r[32];
       if (n > 0) {
-        tmem_ld32(tmem + lane_base + 256 + 128 * ch + 32 * c, r);
+        tmem_ld32(tmem + lane_base + 256 + kOColsPerThread * ch + 32 * c, r);
         tmem_wait_ld();
       }
       if (row_ok) {
@@ -583,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int pair_idx = x % p.n_pairs;
   x /= p.n_pairs;
   const int chunk = x % p.n_chunks;
-  const int b = x / p.n_chunks;
+  const int b = p.order[x / p.n_chunks];
   const int rt = 2 * pair_idx + (int)rank;
 
   const Layout y = layout_of(p, b);   // identical in both CTAs of the pair
@@ -602,8 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.s_full[0], 1);
     mbar_init(&sm.s_full[1], 1);
-    mbar_init(&sm.p_full[0], 16);
-    mbar_init(&sm.p_full[1], 16);
+    mbar_init(&sm.p_full[0], 2);
+    mbar_init(&sm.p_full[1], 2);
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.drain, 1);
@@ -715,10 +750,14 @@ bool tv_tc_available() {
   return cached == 1;
 }
 
+// Workspace: the request order (B int32, padded to 256 B), then the split-KV partials.
+static size_t order_bytes(const tv_shape* s) { return ((size_t)s->B * 4 + 255) / 256 * 256; }
+
 size_t tv_tc_workspace_size(const tv_shape* s) {
   const int n = tc_chunks(s);
-  if (n == 1) return 256;
-  return (size_t)s->B * s->D * s->H * n * (s->d + 4) * sizeof(float);
+  size_t bytes = order_bytes(s);
+  if (n > 1) bytes += (size_t)s->B * s->D * s->H * n * (s->d + 4) * sizeof(float);
+  return bytes;
 }
 
 int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a, void* workspace,
@@ -775,8 +814,12 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.scale_log2 = a.scale_log2;
   p.O = a.O;
   p.lse = a.lse;
-  p.part = reinterpret_cast<float*>(workspace);
+  int32_t* order = reinterpret_cast<int32_t*>(workspace);
+  p.order = order;
+  p.part = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + order_bytes(s));
   p.status = a.status;
+  order_kernel<<<(s->B + 127) / 128, 128, 0, stream>>>(p, order);
+  if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;
   const size_t smem = sizeof(Smem);
   if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)

@@ -17,25 +17,76 @@
 
 namespace tv {
 
-constexpr int kCompressThreads = 128;
+constexpr int kCompressThreads = 256;
+constexpr int kRedFloats = kCompressThreads * 8;   // group partials: blockDim * (16 B / 2 B)
+
+// Vector load of N consecutive elements as fp32.
+template <typename T, int N>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16, 8> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* out) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      out[2 * k] = f.x;
+      out[2 * k + 1] = f.y;
+    }
+  }
+};
+template <>
+struct Vec<float, 4> {
+  static __device__ __forceinline__ void load(const float* p, float* out) {
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    out[0] = f.x;
+    out[1] = f.y;
+    out[2] = f.z;
+    out[3] = f.w;
+  }
+};
+template <typename T>
+struct VecWidth;
+template <>
+struct VecWidth<__nv_bfloat16> {
+  static constexpr int n = 8;
+};
+template <>
+struct VecWidth<float> {
+  static constexpr int n = 4;
+};
 
 // One compressed entry from the m token rows rowK[t] / rowV[t] (t in position order).
-// Whole-CTA routine; w_smem holds m floats.  Reduction orders depend only on the warp size.
+// Whole-CTA routine (kCompressThreads threads); w_smem holds m floats, red 2*kRedFloats.  Reduction orders depend
+// only on the thread layout, which all callers share, so every caller computes bit-identical
+// entries for the same block.  Loads are 16-byte vectors and the token loops are unrolled so that
+// many loads are in flight: a 128-token block is 256 KB of K and V.
 template <typename T>
 __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int m, int d,
-                                const float* __restrict__ g, T* outK, T* outV, float* w_smem) {
+                                const float* __restrict__ g, T* outK, T* outV, float* w_smem,
+                                float* red) {
+  constexpr int VW = VecWidth<T>::n;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
+  // 1. gate logits z_t = K_t . g: warp per token, lanes over 16-byte vectors of the row
+#pragma unroll 4
   for (int t = warp; t < m; t += nwarps) {
     const T* k = rowK[t];
     float acc = 0.f;
-    for (int i = lane; i < d; i += 32) acc = fmaf(load_f(k + i), g[i], acc);
+    for (int i = lane * VW; i < d; i += 32 * VW) {
+      float kv[VW];
+      Vec<T, VW>::load(k + i, kv);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) acc = fmaf(kv[e], g[i + e], acc);
+    }
     acc = warp_sum(acc);
     if (lane == 0) w_smem[t] = acc;
   }
   __syncthreads();
+  // 2. softmax over the m logits
   if (warp == 0) {
     float mx = -INFINITY;
     for (int t = lane; t < m; t += 32) mx = fmaxf(mx, w_smem[t]);
@@ -52,12 +103,42 @@ __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int 
     for (int t = lane; t < m; t += 32) w_smem[t] *= inv;
   }
   __syncthreads();
+  // 3. weighted sums: the threads form G groups of d/VW; thread (group gi, slot li) owns dims
+  //    li*VW .. li*VW+VW-1 and the tokens gi, gi+G, ...; the group partials are then added in
+  //    group order (a fixed order, so the result does not depend on timing)
+  const int per_group = d / VW;
+  int G = blockDim.x / per_group;
+  if (G > m) G = m;
+  const int gi = tid / per_group, li = tid % per_group;
+  if (gi < G) {
+    const int i = li * VW;
+    float ak[VW], av[VW];
+#pragma unroll
+    for (int e = 0; e < VW; ++e) ak[e] = av[e] = 0.f;
+#pragma unroll 4
+    for (int t = gi; t < m; t += G) {
+      const float w = w_smem[t];
+      float kv[VW], vv[VW];
+      Vec<T, VW>::load(rowK[t] + i, kv);
+      Vec<T, VW>::load(rowV[t] + i, vv);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) {
+        ak[e] = fmaf(w, kv[e], ak[e]);
+        av[e] = fmaf(w, vv[e], av[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      red[(gi * d + i + e) * 2] = ak[e];
+      red[(gi * d + i + e) * 2 + 1] = av[e];
+    }
+  }
+  __syncthreads();
   for (int i = tid; i < d; i += blockDim.x) {
     float ak = 0.f, av = 0.f;
-    for (int t = 0; t < m; ++t) {
-      const float w = w_smem[t];
-      ak = fmaf(w, load_f(rowK[t] + i), ak);
-      av = fmaf(w, load_f(rowV[t] + i), av);
+    for (int k = 0; k < G; ++k) {
+      ak += red[(k * d + i) * 2];
+      av += red[(k * d + i) * 2 + 1];
     }
     store_f(outK + i, ak);
     store_f(outV + i, av);
@@ -74,6 +155,7 @@ __global__ void prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
   __shared__ const T* rowK[128];
   __shared__ const T* rowV[128];
   __shared__ float w[128];
+  __shared__ float red[2 * kRedFloats];
   const int b = blockIdx.y;
   const int Lb = L[b];
   if (Lb < 0 || Lb > raw_cap || (int64_t)(Lb / m) > cap_m) {
@@ -89,7 +171,7 @@ __global__ void prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
     }
     __syncthreads();
     const int64_t out = ((int64_t)b * cap_m + j) * d;
-    gated_block_sum<T>(rowK, rowV, m, d, g, CK + out, CV + out, w);
+    gated_block_sum<T>(rowK, rowV, m, d, g, CK + out, CV + out, w, red);
     __syncthreads();
   }
 }
@@ -108,6 +190,7 @@ __global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
   __shared__ const T* rowK[128];
   __shared__ const T* rowV[128];
   __shared__ float w[128];
+  __shared__ float red[2 * kRedFloats];
   __shared__ int path[kMaxD];   // path[k] = ancestor of v at depth k
   __shared__ int s_depth;
   __shared__ int s_ok;
@@ -172,7 +255,7 @@ __global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
     }
   }
   __syncthreads();
-  gated_block_sum<T>(rowK, rowV, m, d, g, outK + out, outV + out, w);
+  gated_block_sum<T>(rowK, rowV, m, d, g, outK + out, outV + out, w, red);
 }
 
 // ---- refresh: commit the accepted path --------------------------------------------------------
