@@ -60,6 +60,8 @@ def parse():
                     help="requests per GPU (default: the workload's own batch)")
     ap.add_argument("--sets", type=int, default=3,
                     help="rotating state copies (3 keeps every step's inputs out of L2)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the five calls directly instead of replaying a captured round")
     return ap.parse_args()
 
 
@@ -377,8 +379,19 @@ def run_ours(args, world, rank, local):
         engine.accept(shape, st, rb, stream)
         engine.refresh(shape, st, rb, stream)
 
+    # the round as a CUDA graph per state copy (the L reset is captured with it); attention time
+    # comes from a separate eager pass with events around the attention launch
+    graphs = None
+    if not args.no_graph:
+        graphs = []
+        for st, rb, L0 in sets:
+            graphs.append(engine.RoundGraph(
+                shape, st, rb, prologue=lambda st=st, L0=L0: st.L.copy_(L0, non_blocking=True)))
     for i in range(args.warmup):
-        step(i)
+        if graphs:
+            graphs[i % n_sets].replay()
+        else:
+            step(i)
     torch.cuda.synchronize()
     barrier(world)
     clocks = ClockSampler(local) if rank == 0 else None
@@ -390,11 +403,18 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start.record(stream)
     for k in range(args.steps):
-        step(args.warmup + k, ev[k])
+        if graphs:
+            graphs[(args.warmup + k) % n_sets].replay()
+        else:
+            step(args.warmup + k, ev[k])
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     barrier(world)
+    if graphs:
+        for k in range(args.steps):
+            step(args.warmup + k, ev[k])
+        torch.cuda.synchronize()
     ms = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms, world)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
@@ -452,7 +472,8 @@ def run_ours(args, world, rank, local):
                    "H": wl.H, "d": wl.d, "attention_kernel": tc_name,
                    "l2": f"inputs larger than L2: {n_sets} rotating state copies, "
                          f"{kv_bytes / 1e6:.0f} MB KV per step each",
-                   "parallelism": f"replicas x{world} (requests sharded, no collective)"},
+                   "parallelism": f"replicas x{world} (requests sharded, no collective)",
+                   "cuda_graph": graphs is not None},
         "roofline": {"bound": "tensor", "achieved": tflops,
                      "peak": pk["tc_sus"], "unit": "TFLOP/s", "frac": tflops / pk["tc_sus"],
                      "traffic": None if traffic is None else traffic["bytes_per_launch"],
@@ -476,8 +497,13 @@ def run_ours(args, world, rank, local):
 
 
 def launches_per_step(shape, kernel):
-    # plan, branch compress, attention (+ merge), accept, refresh
-    return 4 + (2 if kernel == "simt" else 2)
+    # plan, branch compress, accept, refresh + attention: SIMT (partials, merge) or tensor cores
+    # (request ranking, pair kernel, merge when the KV is split)
+    from tree_speculative_verify_gb300 import _lib
+    if kernel == "simt":
+        return 6
+    split = _lib.tv_workspace_size(shape) > ((shape.B * 4 + 255) // 256) * 256
+    return 4 + 2 + (1 if split else 0)
 
 
 def main():

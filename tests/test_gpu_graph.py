@@ -1,0 +1,55 @@
+"""A verify round captured as a CUDA graph gives the eager round's results, replay after replay.
+
+"Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for Efficient Inference" §4.3 replays
+the verification step as a CUDA graph.  The round's five calls are captured once on fixed buffers
+(with the reset of the committed lengths as a prologue, so every replay verifies the same tree
+from the same prefix); every output of every replay must equal, bit for bit, what one eager round
+on a copy of the same state produced: the graph runs the same kernels on the same data.
+"""
+
+import pytest
+import torch
+
+from tree_speculative_verify_gb300 import _lib, engine, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _outputs(st, rb):
+    return {"O": rb.O, "lse": rb.lse, "accept_len": rb.accept_len, "path": rb.path,
+            "bonus": rb.bonus, "committed": rb.committed, "anc": rb.anc, "vis4": rb.vis4,
+            "vis128": rb.vis128, "scrK4": rb.scrK4, "scrK128": rb.scrK128, "L": st.L,
+            "rawK": st.rawK, "rawV": st.rawV, "c4K": st.c4K, "c4V": st.c4V, "c128K": st.c128K,
+            "c128V": st.c128V}
+
+
+@pytest.mark.parametrize("kernel", [_lib.TV_ATTN_AUTO, _lib.TV_ATTN_SIMT])
+@pytest.mark.parametrize("case", ["small", "serving_reduced"])
+def test_round_graph_replays_match_eager(case, kernel):
+    wl = workloads.small() if case == "small" else workloads.serving(B=8)
+    shape = engine.shape_for(wl, kernel)
+    st = engine.alloc_state(wl)
+    rb = engine.alloc_round(wl, shape)
+    engine.prefill(shape, st, rb)
+    torch.cuda.synchronize()
+    st_eager = st.clone()
+    rb_eager = engine.alloc_round(wl, shape)
+    L0 = st.L.clone()
+
+    engine.verify_round(shape, st_eager, rb_eager)
+    torch.cuda.synchronize()
+    assert int(rb_eager.status.item()) == 0
+    want = {k: v.clone() for k, v in _outputs(st_eager, rb_eager).items()}
+
+    graph = engine.RoundGraph(shape, st, rb, prologue=lambda: st.L.copy_(L0, non_blocking=True))
+    for _ in range(3):
+        for t in (rb.O, rb.lse):
+            t.fill_(float("nan"))
+        for t in (rb.accept_len, rb.path, rb.bonus, rb.committed):
+            t.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(rb.status.item()) == 0
+        got = _outputs(st, rb)
+        for k, v in want.items():
+            assert torch.equal(got[k], v), f"{k} differs after a graph replay"

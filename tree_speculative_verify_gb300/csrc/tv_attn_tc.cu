@@ -142,15 +142,15 @@ __device__ __forceinline__ Tile tile_of(const Layout& y, int t) {
 // requests first, so the last wave holds the shortest work items.  rank(b) = number of requests
 // with more tiles, ties broken by index; order[rank(b)] = b.
 __global__ void order_kernel(Params p, int32_t* order) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= p.B) return;
-  const int tb = layout_of(p, b).T;
-  int rank = 0;
-  for (int j = 0; j < p.B; ++j) {
-    const int tj = layout_of(p, j).T;
-    rank += (tj > tb || (tj == tb && j < b)) ? 1 : 0;
+  extern __shared__ int tiles[];   // B tile counts
+  for (int j = threadIdx.x; j < p.B; j += blockDim.x) tiles[j] = layout_of(p, j).T;
+  __syncthreads();
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const int tb = tiles[b];
+    int rank = 0;
+    for (int j = 0; j < p.B; ++j) rank += (tiles[j] > tb || (tiles[j] == tb && j < b)) ? 1 : 0;
+    order[rank] = b;
   }
-  order[rank] = b;
 }
 
 struct __align__(1024) Smem {
@@ -731,6 +731,7 @@ int tc_chunks(const tv_shape* s) {
 
 bool tv_tc_shape_ok(const tv_shape* s) {
   return s->dtype == TV_BF16 && s->d == 512 && s->D <= tv::tc::kDp && s->n_sel == 0 &&
+         s->B <= 12288 &&   // the ranking kernel keeps one int per request in shared memory
          (int64_t)s->B * s->raw_cap < ((int64_t)1 << 31) &&
          (int64_t)s->B * s->c4_cap < ((int64_t)1 << 31) &&
          (int64_t)s->B * s->c128_cap < ((int64_t)1 << 31);
@@ -818,12 +819,25 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.order = order;
   p.part = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + order_bytes(s));
   p.status = a.status;
-  order_kernel<<<(s->B + 127) / 128, 128, 0, stream>>>(p, order);
+  // one CTA ranks all requests (B <= 12288 fits its default shared memory)
+  order_kernel<<<1, 1024, (size_t)s->B * sizeof(int), stream>>>(p, order);
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;
   const size_t smem = sizeof(Smem);
-  if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return tv_check_launch("tv_tree_verify_attn (tcgen05 shared-memory attribute)");
+  // once per device (a plain host call that also stays out of any stream being captured)
+  static std::mutex attr_mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return tv_check_launch("tv_tree_verify_attn (tcgen05 device query)");
+  {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess)
+        return tv_check_launch("tv_tree_verify_attn (tcgen05 shared-memory attribute)");
+      attr_set[dev] = true;
+    }
+  }
   const unsigned grid = (unsigned)(s->B * p.n_chunks * p.n_pairs * 4);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -17,8 +17,9 @@
 
 namespace tv {
 
-constexpr int kCompressThreads = 256;
+constexpr int kCompressThreads = 512;
 constexpr int kRedFloats = kCompressThreads * 8;   // group partials: blockDim * (16 B / 2 B)
+static_assert(2 * kRedFloats * 4 <= 40 * 1024, "group partials must fit static shared memory");
 
 // Vector load of N consecutive elements as fp32.
 template <typename T, int N>
@@ -58,9 +59,9 @@ struct VecWidth<float> {
 };
 
 // One compressed entry from the m token rows rowK[t] / rowV[t] (t in position order).
-// Whole-CTA routine (kCompressThreads threads); w_smem holds m floats, red 2*kRedFloats.  Reduction orders depend
-// only on the thread layout, which all callers share, so every caller computes bit-identical
-// entries for the same block.  Loads are 16-byte vectors and the token loops are unrolled so that
+// Whole-CTA routine (kCompressThreads threads); w_smem holds m floats, red 2*kRedFloats.
+// Reduction orders depend only on the thread layout, which all callers share, so every caller
+// computes bit-identical entries for the same block.  Loads are 16-byte vectors and the token loops are unrolled so that
 // many loads are in flight: a 128-token block is 256 KB of K and V.
 template <typename T>
 __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int m, int d,
@@ -259,14 +260,9 @@ __global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
 }
 
 // ---- refresh: commit the accepted path --------------------------------------------------------
-// One CTA per request.  Copies the accepted tokens' K/V into the raw rows L .. L+n-1, copies the
-// scratch rows of accepted nodes that close a block into the persistent entries, advances L.
-__device__ __forceinline__ void copy_row(void* dst, const void* src, int bytes) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) d4[i] = s4[i];
-}
-
+// One CTA per request.  Copies the accepted tokens' K/V into the raw rows L .. L+n-1 and the
+// scratch rows of accepted nodes that close a block into the persistent entries (all rows in
+// parallel: each 16-byte chunk of each row is one thread's job), then advances L.
 __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_cap,
                                int64_t c4_cap, int64_t c128_cap,
                                const int32_t* __restrict__ accept_len,
@@ -275,9 +271,15 @@ __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_
                                const char* scrK128, const char* scrV128, char* rawK, char* rawV,
                                char* c4K, char* c4V, char* c128K, char* c128V, int32_t* L,
                                int32_t* committed, int32_t* status) {
+  constexpr int kMaxJobs = 3 * kMaxD;   // raw rows + C4 entries + C128 entries
   __shared__ int s_ok;
   __shared__ int s_L;
   __shared__ int s_n;
+  __shared__ int s_jobs;
+  __shared__ const char* s_srcK[kMaxJobs];
+  __shared__ const char* s_srcV[kMaxJobs];
+  __shared__ char* s_dstK[kMaxJobs];
+  __shared__ char* s_dstV[kMaxJobs];
   const int b = blockIdx.x;
   const int64_t row_bytes = (int64_t)d * es;
   const int32_t* path = path_all + (int64_t)b * D;
@@ -295,9 +297,39 @@ __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_
       if ((comp_mask & TV_COMP_C128) && Lnew / 128 > c128_cap) { ok = 0; code = TV_ERR_CAPACITY; }
     }
     if (!ok) record_error(status, code);
+    int jobs = 0;
+    if (ok) {
+      for (int i = 0; i < n; ++i) {
+        const int64_t src = ((int64_t)b * D + path[i]) * row_bytes;
+        const int64_t dst = ((int64_t)b * raw_cap + Lb + i) * row_bytes;
+        s_srcK[jobs] = treeK + src;
+        s_srcV[jobs] = treeV + src;
+        s_dstK[jobs] = rawK + dst;
+        s_dstV[jobs] = rawV + dst;
+        ++jobs;
+        const int e = Lb + i;
+        if ((comp_mask & TV_COMP_C4) && ((e + 1) & 3) == 0) {
+          const int64_t cd = ((int64_t)b * c4_cap + (e + 1) / 4 - 1) * row_bytes;
+          s_srcK[jobs] = scrK4 + src;
+          s_srcV[jobs] = scrV4 + src;
+          s_dstK[jobs] = c4K + cd;
+          s_dstV[jobs] = c4V + cd;
+          ++jobs;
+        }
+        if ((comp_mask & TV_COMP_C128) && ((e + 1) & 127) == 0) {
+          const int64_t cd = ((int64_t)b * c128_cap + (e + 1) / 128 - 1) * row_bytes;
+          s_srcK[jobs] = scrK128 + src;
+          s_srcV[jobs] = scrV128 + src;
+          s_dstK[jobs] = c128K + cd;
+          s_dstV[jobs] = c128V + cd;
+          ++jobs;
+        }
+      }
+    }
     s_ok = ok;
     s_L = Lb;
     s_n = n;
+    s_jobs = jobs;
   }
   __syncthreads();
   int32_t* cpos = committed + (int64_t)b * D;
@@ -305,30 +337,16 @@ __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_
     for (int i = threadIdx.x; i < D; i += blockDim.x) cpos[i] = -1;
     return;
   }
-  const int Lb = s_L, n = s_n;
-  for (int i = 0; i < n; ++i) {
-    const int64_t src = ((int64_t)b * D + path[i]) * row_bytes;
-    const int64_t dst = ((int64_t)b * raw_cap + Lb + i) * row_bytes;
-    copy_row(rawK + dst, treeK + src, (int)row_bytes);
-    copy_row(rawV + dst, treeV + src, (int)row_bytes);
+  const int chunks = (int)(row_bytes / 16);
+  const int total = s_jobs * chunks;
+  for (int k = threadIdx.x; k < total; k += blockDim.x) {
+    const int j = k / chunks, c = k - j * chunks;
+    reinterpret_cast<uint4*>(s_dstK[j])[c] = reinterpret_cast<const uint4*>(s_srcK[j])[c];
+    reinterpret_cast<uint4*>(s_dstV[j])[c] = reinterpret_cast<const uint4*>(s_srcV[j])[c];
   }
-  for (int e = Lb; e < Lb + n; ++e) {
-    const int u = path[e - Lb];
-    const int64_t src = ((int64_t)b * D + u) * row_bytes;
-    if ((comp_mask & TV_COMP_C4) && ((e + 1) & 3) == 0) {
-      const int64_t dst = ((int64_t)b * c4_cap + (e + 1) / 4 - 1) * row_bytes;
-      copy_row(c4K + dst, scrK4 + src, (int)row_bytes);
-      copy_row(c4V + dst, scrV4 + src, (int)row_bytes);
-    }
-    if ((comp_mask & TV_COMP_C128) && ((e + 1) & 127) == 0) {
-      const int64_t dst = ((int64_t)b * c128_cap + (e + 1) / 128 - 1) * row_bytes;
-      copy_row(c128K + dst, scrK128 + src, (int)row_bytes);
-      copy_row(c128V + dst, scrV128 + src, (int)row_bytes);
-    }
-  }
-  for (int i = threadIdx.x; i < D; i += blockDim.x) cpos[i] = i < n ? Lb + i : -1;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) cpos[i] = i < s_n ? s_L + i : -1;
   __syncthreads();
-  if (threadIdx.x == 0) L[b] = Lb + n;
+  if (threadIdx.x == 0) L[b] = s_L + s_n;
 }
 
 }  // namespace tv
@@ -396,7 +414,7 @@ int tv_launch_refresh(const tv_shape* s, const int32_t* accept_len, const int32_
                       void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
                       int32_t* committed, int32_t* status, cudaStream_t stream) {
   const int es = s->dtype == TV_BF16 ? 2 : 4;
-  tv::refresh_kernel<<<s->B, 128, 0, stream>>>(
+  tv::refresh_kernel<<<s->B, 256, 0, stream>>>(
       s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap, accept_len, path,
       (const char*)treeK, (const char*)treeV, (const char*)scrK4, (const char*)scrV4,
       (const char*)scrK128, (const char*)scrV128, (char*)rawK, (char*)rawV, (char*)c4K,

@@ -160,3 +160,28 @@ def verify_round(shape, st, rb, scale=None, stream=None, commit=True):
     accept(shape, st, rb, stream)
     if commit:
         refresh(shape, st, rb, stream)
+
+
+class RoundGraph:
+    """One verify round captured as a CUDA graph on fixed buffers.
+
+    "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for Efficient Inference" §4.3
+    replays the verification step as a CUDA graph sized for the tree configuration; here the five
+    calls (and an optional ``prologue`` of stream work, e.g. refilling inputs) are captured once
+    and ``replay()`` relaunches them with a single graph launch.  The buffers in ``st`` / ``rb``
+    must stay allocated and at the same addresses; their contents may change between replays.
+    """
+
+    def __init__(self, shape, st, rb, scale=None, commit=True, prologue=None):
+        # one eager round first: per-device set-up of the library happens outside the capture
+        verify_round(shape, st, rb, scale, None, commit)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            stream = torch.cuda.current_stream()
+            if prologue is not None:
+                prologue()
+            verify_round(shape, st, rb, scale, stream, commit)
+
+    def replay(self):
+        self.graph.replay()
