@@ -195,34 +195,46 @@ __device__ __forceinline__ bool entry_visible(const EntryRef& r, const NodeVis& 
   return entry_visible_kind(r.kind, r.aux, n);
 }
 
-// Split-KV merge: one warp per (request, node, head) row.
+// Split-KV merge: one block per (request, node, head) row, d/4 threads; thread t owns columns
+// 4t .. 4t+3.  Every thread derives the chunk weights itself (a few dozen broadcast loads), so
+// the column loads of all chunks are independent and the row needs no block synchronisation.
+// Chunk rows are d + 4 floats (16-byte aligned for d a multiple of 8): O partial, m (log2
+// units), l.
 template <typename T>
 __global__ void merge_kernel(int rows, int d, int n_chunks, const float* __restrict__ part,
                              T* __restrict__ O, float* __restrict__ lse) {
-  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x;
   if (row >= rows) return;
-  const float* pr = part + (int64_t)row * n_chunks * (d + 4);
+  const int64_t stride = d + 4;
+  const float* pr = part + (int64_t)row * n_chunks * stride;
   float M = -INFINITY;
-  for (int c = 0; c < n_chunks; ++c) {
-    const float* pc = pr + (int64_t)c * (d + 4);
-    if (pc[d + 1] > 0.f) M = fmaxf(M, pc[d]);
-  }
+  for (int c = 0; c < n_chunks; ++c)
+    if (pr[c * stride + d + 1] > 0.f) M = fmaxf(M, pr[c * stride + d]);
   float denom = 0.f;
-  for (int c = 0; c < n_chunks; ++c) {
-    const float* pc = pr + (int64_t)c * (d + 4);
-    if (pc[d + 1] > 0.f) denom += exp2f(pc[d] - M) * pc[d + 1];
-  }
+  for (int c = 0; c < n_chunks; ++c)
+    if (pr[c * stride + d + 1] > 0.f) denom += exp2f(pr[c * stride + d] - M) * pr[c * stride + d + 1];
   const float inv = denom > 0.f ? 1.f / denom : 0.f;
-  for (int i = lane; i < d; i += 32) {
-    float acc = 0.f;
+  for (int i = 4 * threadIdx.x; i < d; i += 4 * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = 0; c < n_chunks; ++c) {
-      const float* pc = pr + (int64_t)c * (d + 4);
-      if (pc[d + 1] > 0.f) acc += exp2f(pc[d] - M) * pc[i];
+      const float* pc = pr + c * stride;
+      if (pc[d + 1] > 0.f) {
+        const float w = exp2f(pc[d] - M);
+        const float4 v = *reinterpret_cast<const float4*>(pc + i);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
     }
-    store_f(O + (int64_t)row * d + i, acc * inv);
+    T* o = O + (int64_t)row * d + i;
+    store_f(o, acc.x * inv);
+    store_f(o + 1, acc.y * inv);
+    store_f(o + 2, acc.z * inv);
+    store_f(o + 3, acc.w * inv);
   }
-  if (lane == 0) lse[row] = denom > 0.f ? (M + log2f(denom)) * 0.6931471805599453f : -INFINITY;
+  if (threadIdx.x == 0)
+    lse[row] = denom > 0.f ? (M + log2f(denom)) * 0.6931471805599453f : -INFINITY;
 }
 
 }  // namespace tv
@@ -231,9 +243,8 @@ template <typename T>
 int tv_launch_merge(int B, int DH, int d, int n_chunks, const float* part, T* O, float* lse,
                     cudaStream_t stream) {
   const int rows = B * DH;
-  const int warps = 8;
-  tv::merge_kernel<T><<<(rows + warps - 1) / warps, warps * 32, 0, stream>>>(rows, d, n_chunks,
-                                                                              part, O, lse);
+  const int threads = d / 4 < 32 ? 32 : (d / 4 > 256 ? 256 : d / 4);
+  tv::merge_kernel<T><<<rows, threads, 0, stream>>>(rows, d, n_chunks, part, O, lse);
   return tv_check_launch("tv_tree_verify_attn (merge)");
 }
 

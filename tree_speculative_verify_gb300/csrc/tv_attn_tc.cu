@@ -22,10 +22,10 @@
 // to every row; raw and extra tiles are filtered per tree node with the plan (raw_lo, ancestor
 // mask, scratch visibility) inside the softmax warps.
 //
-// Warp roles (320 threads per CTA):
-//   warp 0      TMA producer: Q once (8 boxes of 128 x 64); then, through a 6-slot ring of 16 KB,
-//               this CTA's share of every tile: for S, two 64-dim slices of N/2 entries; for PV,
-//               64 entries x 128 value columns
+// Warp roles (352 threads per CTA):
+//   warp 0      TMA producer: Q once (8 boxes of 128 x 64); then, through a 3-slot ring of 32 KB,
+//               this CTA's share of every tile: for S, two slots of four 64-dim slices of N/2
+//               entries; for PV, one slot of the tile's entries x 128 value columns
 //   warp 1      both CTAs: allocate / free 512 TMEM columns (cta_group::2).  Leader lane 0 issues
 //               S_t = Q K_t^T  (M=256, N=entries rounded to 16, K=512; A and B K-major)
 //               O  += P_t V_t   (M=256, N=256, K=entries; A = P in TMEM, B = V MN-major)
@@ -35,6 +35,8 @@
 //               from TMEM, mask, online softmax with a lazily updated row maximum, write P_t back
 //               into the S columns as packed bf16, rescale O in TMEM when the maximum grows by
 //               more than 2^8, and finally write O.
+//   warp 10     lane 0: once every softmax warp of the CTA has stored P_t, arrives on the
+//               leader's p_full (a cluster-scope release that stalls its thread for a while).
 // TMEM columns: S/P double buffer at [0,128) and [128,256), O at [256,512).
 // Every mbarrier wait is bounded; on timeout the CTA records TV_ERR_TIMEOUT, stops issuing work,
 // drains its own copies and MMAs (bounded) and frees its TMEM.
@@ -53,9 +55,15 @@ namespace tc {
 using namespace sm100;
 
 constexpr int kSmxWarps = 8;           // softmax warps: 4 (a thread per row) or 8 (two per row)
-constexpr int kThreads = 64 + 32 * kSmxWarps;   // producer, MMA issuer, softmax warps
-constexpr int kSlots = 6;
-constexpr int kSlotBytes = 16384;
+constexpr int kSigWarp = 2 + kSmxWarps;          // forwards "P ready" to the leader
+constexpr int kThreads = 64 + 32 * kSmxWarps + 32;   // producer, MMA issuer, softmax, signal
+// Ring of 32 KB slots: the rate at which one SM's TMA copies complete is set mostly by the
+// number of mbarrier transactions (about 0.3 us each, nearly independent of their size up to
+// 64 KB), so a tile's K share (64 KB) takes two slots and its V share (32 KB) one.
+constexpr int kSlots = 3;
+constexpr int kSlotBytes = 32768;
+constexpr int kKSlices = 4;        // 64-dim K slices (64 entries x 128 B, 8 KB) per slot
+constexpr int kVBlock = 16384;     // V slot: two 64-column blocks of 128 entries
 constexpr int kQBytes = 8 * 16384;
 constexpr int kDp = 8;                 // rows per section of the extra tile (D <= 8)
 constexpr int kExtraEntries = 32;      // tree | C4 scratch | C128 scratch | zeros
@@ -161,6 +169,7 @@ struct __align__(1024) Smem {
   uint64_t q_full;
   uint64_t s_full[2];
   uint64_t p_full[2];          // (leader) P written by both CTAs' softmax warps
+  uint64_t p_local[2];         // this CTA's softmax warps have written P (one arrive per warp)
   uint64_t pv_done;
   uint64_t o_full;
   uint64_t drain;
@@ -218,19 +227,19 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
     if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
   };
   // S operand: this CTA holds entries [rank * nqk/2, (rank+1) * nqk/2) of the tile; one slot
-  // holds two 64-dim slices of those (up to 64) entries, 8 KB each.
+  // holds four 64-dim slices of those (up to 64) entries, 8 KB each.
   auto load_k = [&](const Tile& x) -> bool {
     const int nh = x.nqk / 2;
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 512 / (64 * kKSlices); ++j) {
       if (!acquire()) return false;
       if (lane == 0) {
         uint8_t* dst = sm.ring[slot];
         const uint32_t bar = leader_full(slot);
         if (x.kind == kExtra) {
           // leader: tree rows | C4 scratch rows; follower: C128 scratch rows | zero rows
-          expect(2 * 2 * kDp * 128);
-          for (int ks = 0; ks < 2; ++ks) {
-            const int xcol = 64 * (2 * j + ks);
+          expect(kKSlices * 2 * kDp * 128);
+          for (int ks = 0; ks < kKSlices; ++ks) {
+            const int xcol = 64 * (kKSlices * j + ks);
             uint8_t* d = dst + ks * 8192;
             if (rank == 0) {
               tma_load_2d_pair(d, &p.mTreeK, xcol, tree_row, bar);
@@ -244,8 +253,8 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
           const CUtensorMap* m = x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
           const int r = (int)(base_row(p, x.kind, b) + x.row0 + (int)rank * nh);
           expect(kSlotBytes);
-          tma_load_2d_pair(dst, m, 64 * (2 * j), r, bar);
-          tma_load_2d_pair(dst + 8192, m, 64 * (2 * j + 1), r, bar);
+          for (int ks = 0; ks < kKSlices; ++ks)
+            tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * j + ks), r, bar);
         }
       }
       advance();
@@ -253,11 +262,12 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
     return true;
   };
   // PV operand: every entry of the tile, this CTA's 128 of the pair's 256 value columns; one slot
-  // holds 64 entries as two 64-column blocks of 64 rows.
+  // holds the tile's entries as two 64-column blocks of 128 rows (rows past the tile's entry
+  // count rounded up to 64 are not loaded).
   auto load_v = [&](const Tile& x) -> bool {
-    const int nvs = (x.nqk + 63) / 64;
+    const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
     const int col0 = 256 * half + 128 * (int)rank;
-    for (int j = 0; j < nvs; ++j) {
+    {
       if (!acquire()) return false;
       if (lane == 0) {
         uint8_t* dst = sm.ring[slot];
@@ -265,7 +275,7 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
         if (x.kind == kExtra) {
           expect(2 * 4 * kDp * 128);
           for (int cb = 0; cb < 2; ++cb) {
-            uint8_t* d = dst + cb * 8192;
+            uint8_t* d = dst + cb * kVBlock;
             const int xc = col0 + 64 * cb;
             tma_load_2d_pair(d, &p.mTreeV, xc, tree_row, bar);
             tma_load_2d_pair(d + kDp * 128, &p.mS4V, xc, tree_row, bar);
@@ -274,10 +284,11 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
           }
         } else {
           const CUtensorMap* m = x.kind == kC4 ? &p.mC4V : x.kind == kC128 ? &p.mC128V : &p.mRawV;
-          const int r = (int)(base_row(p, x.kind, b) + x.row0 + 64 * j);
-          expect(kSlotBytes);
-          tma_load_2d_pair(dst, m, col0, r, bar);
-          tma_load_2d_pair(dst + 8192, m, col0 + 64, r, bar);
+          const int r = (int)(base_row(p, x.kind, b) + x.row0);
+          expect(nvh * 2 * 8192);
+          for (int h = 0; h < nvh; ++h)
+            for (int cb = 0; cb < 2; ++cb)
+              tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb, r + 64 * h, bar);
         }
       }
       advance();
@@ -336,14 +347,11 @@ __device__ void mma_issuer(const Params& p, Smem& sm, const Layout& y, int tb, i
     }
     tc_fence_after();
     const int nks = x.nqk / 16;
-    const int nvs = (x.nqk + 63) / 64;
-    for (int vs = 0; vs < nvs; ++vs) {
+    {
       if (!wait_slot()) return false;
       const uint32_t vbase = smem_u32(sm.ring[slot]);
-      for (int kk = 0; kk < 4; ++kk) {
-        const int ks = 4 * vs + kk;
-        if (ks >= nks) break;
-        const uint64_t bdesc = smem_desc_sw128(vbase + 2048 * kk, 8192, 1024);
+      for (int ks = 0; ks < nks; ++ks) {
+        const uint64_t bdesc = smem_desc_sw128(vbase + 2048 * ks, kVBlock, 1024);
         mma2_ts(tmem + 256, tmem + 128 * (j & 1) + 8 * ks, bdesc, idO, (j > 0 || ks > 0) ? 1u : 0u);
       }
       release();
@@ -356,15 +364,15 @@ __device__ void mma_issuer(const Params& p, Smem& sm, const Layout& y, int tb, i
     const Tile x = tile_of(y, tb + i);
     const uint32_t idS = idesc_bf16_f32(256, x.nqk, 0, 0);
     const uint32_t d_s = tmem + 128 * (i & 1);
-    for (int j = 0; j < 4 && ok; ++j) {
+    for (int j = 0; j < 512 / (64 * kKSlices) && ok; ++j) {
       if (!wait_slot()) {
         ok = false;
         break;
       }
       const uint32_t kbase = smem_u32(sm.ring[slot]);
-      for (int ks = 0; ks < 2; ++ks)
+      for (int ks = 0; ks < kKSlices; ++ks)
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc_sw128(q_base + (2 * j + ks) * 16384 + 32 * kk, 16, 1024);
+          const uint64_t a = smem_desc_sw128(q_base + (kKSlices * j + ks) * 16384 + 32 * kk, 16, 1024);
           const uint64_t bd = smem_desc_sw128(kbase + ks * 8192 + 32 * kk, 16, 1024);
           mma2_ss(d_s, a, bd, idS, (j | ks | kk) ? 1u : 0u);
         }
@@ -394,9 +402,22 @@ constexpr int kOColsPerThread = 256 / kCh;  // O columns per thread
 __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
-// all softmax warps of this CTA
-__device__ __forceinline__ void softmax_sync() {
-  asm volatile("bar.sync 5, %0;" ::"n"(kSmxWarps * 32) : "memory");
+
+// ---- signal warp: P of tile i is in both CTAs' TMEM -> the leader's MMA issuer ----------------
+// Lane 0 waits until all softmax warps of this CTA have stored P_i (local barrier), then performs
+// the release-arrive at cluster scope on the leader's p_full.  That remote arrive stalls its
+// thread for several hundred nanoseconds, which would otherwise delay the next tile's softmax.
+__device__ void p_signal(const Params& p, Smem& sm, int n) {
+  const uint32_t p_full_leader[2] = {mapa_cluster(smem_u32(&sm.p_full[0]), 0),
+                                     mapa_cluster(smem_u32(&sm.p_full[1]), 0)};
+  for (int i = 0; i < n; ++i) {
+    const int sb = i & 1;
+    if (!mbar_wait(&sm.p_local[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs)) {
+      fail(sm, p.status);
+      return;
+    }
+    mbar_arrive_cluster(p_full_leader[sb]);
+  }
 }
 
 __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int half, int chunk,
@@ -410,8 +431,6 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
   const uint32_t tmem = sm.tmem;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const float sl2 = p.scale_log2;
-  const uint32_t p_full_leader[2] = {mapa_cluster(smem_u32(&sm.p_full[0]), 0),
-                                     mapa_cluster(smem_u32(&sm.p_full[1]), 0)};
 
   // per-row visibility of the raw tail and of the extra tile
   int raw_lo = 0;
@@ -531,8 +550,10 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
     m_ref = m_new;
     tmem_wait_st();
     tc_fence_before();
-    softmax_sync();   // one release-arrive per CTA: P of all 128 rows is in TMEM
-    if (warp == 2 && lane == 0) mbar_arrive_cluster(p_full_leader[sb]);
+    // each warp's rows of P are in TMEM; the signal warp forwards the CTA's readiness to the
+    // leader, so no softmax warp waits for the cross-CTA arrive
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.p_local[sb]);
   }
   if (ok && n > 0) {
     if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, 0, &sm.abort, kTimeoutNs))) {
@@ -639,6 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     mbar_init(&sm.s_full[1], 1);
     mbar_init(&sm.p_full[0], 2);
     mbar_init(&sm.p_full[1], 2);
+    mbar_init(&sm.p_local[0], kSmxWarps);
+    mbar_init(&sm.p_local[1], kSmxWarps);
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.drain, 1);
@@ -666,10 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (rank == 0) mma_issuer(p, sm, y, tb, te);
       }
       __syncwarp();
+    } else if (warp == kSigWarp) {
+      if (lane == 0) p_signal(p, sm, te - tb);
+      __syncwarp();
     } else {
       softmax_epilogue(p, sm, b, rt, half, chunk, y, tb, te);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < kSigWarp) {
     softmax_epilogue(p, sm, b, rt, half, chunk, y, tb, te);   // empty chunk: l = 0
   }
 
