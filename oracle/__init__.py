@@ -24,6 +24,7 @@ verify    branch-aware causal attention of every tree node over its visible set
 accept    the greedy acceptance walk
 refresh   accepted-path commit of raw K/V and completed compressed blocks
 round     one full verify round: the five steps above in order
+indexer   top-k selection of persistent C4 entries by an fp32 indexer score (sparse C4 path)
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (``tests/test_oracle_*.py``) against brute force, closed forms, special cases or library
@@ -44,6 +45,7 @@ from .verify import (
 from .accept import accept_walk
 from .refresh import refresh_commit_request
 from .round import verify_round
+from .indexer import index_scores, topk_ascending, indexer_select
 
 __all__ = [
     "round_to_storage",
@@ -62,4 +64,7 @@ __all__ = [
     "accept_walk",
     "refresh_commit_request",
     "verify_round",
+    "index_scores",
+    "topk_ascending",
+    "indexer_select",
 ]
