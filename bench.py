@@ -41,7 +41,8 @@ WORKLOAD_DESC = {
     "serving": "serving batch: B=64, L~U{1024..8192}, D=8 (top-2 tree, 4 steps), H=64x1, d=512, "
                "C4+C128+W128, bf16",
     "small": "small: B=4, L=4096, D=6 (top-2, depth 3), H=64x1, d=512, C4+C128+W128, bf16",
-    "long": "long context: B=8, L~U{65536..131072}, C128 + top-2048 C4, W128, D=8, H=64x1, "
+    "long": "long context: B=8, L~U{65536..131072}, C128 + top-2048 C4 (device indexer in the "
+            "round), W128, D=8, H=64x1, "
             "d=512, bf16",
     "tiny": "tiny fp32: B=1, L=256, C4 only, remainder tail, D=5, H=8x1, d=64",
 }
@@ -400,9 +401,13 @@ def run_ours(args, world, rank, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
 
+    select = shape.n_sel > 0   # the sparse path picks its C4 entries on the device each round
+
     def step(i, timed=None):
         st, rb, L0 = sets[i % n_sets]
         st.L.copy_(L0, non_blocking=True)
+        if select:
+            engine.indexer(shape, st, rb, stream)
         engine.plan(shape, st, rb, stream)
         engine.branch_compress(shape, st, rb, stream)
         if timed is not None:
@@ -420,7 +425,8 @@ def run_ours(args, world, rank, local):
         graphs = []
         for st, rb, L0 in sets:
             graphs.append(engine.RoundGraph(
-                shape, st, rb, prologue=lambda st=st, L0=L0: st.L.copy_(L0, non_blocking=True)))
+                shape, st, rb, prologue=lambda st=st, L0=L0: st.L.copy_(L0, non_blocking=True),
+                select=select))
     for i in range(args.warmup):
         if graphs:
             graphs[i % n_sets].replay()
@@ -458,7 +464,7 @@ def run_ours(args, world, rank, local):
 
     # end to end through the C ABI: inputs from pinned host memory, outputs back to the host
     st, rb, L0 = sets[0]
-    ins = [rb.Q, rb.treeK, rb.treeV, rb.parents, rb.draft, rb.target]
+    ins = [rb.Q, rb.treeK, rb.treeV, rb.parents, rb.draft, rb.target] + ([rb.q_idx] if select else [])
     outs = [rb.O, rb.lse, rb.accept_len, rb.path, rb.bonus, rb.committed]
     host_in = [t.cpu().pin_memory() for t in ins]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
@@ -468,9 +474,10 @@ def run_ours(args, world, rank, local):
     def e2e_step(i):
         s_, r_, l_ = sets[i % n_sets]
         s_.L.copy_(l_, non_blocking=True)
-        for dst, src in zip([r_.Q, r_.treeK, r_.treeV, r_.parents, r_.draft, r_.target], host_in):
+        dsts = [r_.Q, r_.treeK, r_.treeV, r_.parents, r_.draft, r_.target]
+        for dst, src in zip(dsts + ([r_.q_idx] if select else []), host_in):
             dst.copy_(src, non_blocking=True)
-        engine.verify_round(shape, s_, r_, None, stream)
+        engine.verify_round(shape, s_, r_, None, stream, select=select)
         for dst, src in zip(host_out, [r_.O, r_.lse, r_.accept_len, r_.path, r_.bonus, r_.committed]):
             dst.copy_(src, non_blocking=True)
 
@@ -598,13 +605,17 @@ def run_sweep(args):
 
 
 def launches_per_step(shape, kernel):
-    # plan, branch compress, accept, refresh + attention: SIMT (partials, merge) or tensor cores
-    # (request ranking, pair kernel, merge when the KV is split)
+    # plan, branch compress, accept, refresh + attention: SIMT (partials, merge; + the indexer's
+    # two kernels on the sparse path) or tensor cores
+    # (selection gather when a C4 selection list is given, request ranking, pair kernel, merge
+    # when the KV is split)
     from tree_speculative_verify_gb300 import _lib
     if kernel == "simt":
-        return 6
-    split = _lib.tv_workspace_size(shape) > ((shape.B * 4 + 255) // 256) * 256
-    return 4 + 2 + (1 if split else 0)
+        return 6 + (2 if shape.n_sel > 0 else 0)
+    gather = shape.B * shape.n_sel * 512 * 2 * 2
+    split = _lib.tv_workspace_size(shape) > ((shape.B * 4 + 255) // 256) * 256 + gather
+    # + the indexer's score and select kernels and the selection gather on the sparse path
+    return 4 + 2 + (1 if split else 0) + (3 if shape.n_sel > 0 else 0)
 
 
 def main():

@@ -251,6 +251,29 @@ int tv_refresh_commit(const tv_shape* shape, const int32_t* accept_len, const in
                       void* rawV, void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
                       int32_t* committed_pos, int32_t* status, tv_stream_t stream);
 
+/*
+ * Indexer top-k selection of the persistent C4 entries for the sparse prefix path ([TSD-V4] §2.2:
+ * CSA is compressed *sparse* attention; the report gives no selection rule, so the rule here is
+ * the stand-in of the long-context workload).  For every request b with n4 = L[b]/4 C4 entries:
+ *   score[j] = q_idx[b] . k_idx[b][j], j < n4, computed in fp32 as products of the bf16 inputs
+ *   (exact) added in index order 0 .. d_idx-1, one round-to-nearest-even per addition, no fused
+ *   multiply-add;
+ *   sel[b] = the n_sel entries of largest score (equal scores: lower j first), ascending in j --
+ *   the selection list tv_tree_verify_attn takes.
+ * Uses shape->B, c4_cap (rows of k_idx per request), n_sel (> 0) and needs C4 in comp_mask.
+ *   d_idx: indexer dimension, a multiple of 8 in 8..256
+ *   q_idx [B][d_idx] bf16 in; k_idx [B][c4_cap][d_idx] bf16 in (16-byte aligned); L [B] in
+ *   sel [B][n_sel] int32 out
+ *   workspace: device buffer of ws_bytes >= tv_indexer_workspace_size(shape) (the fp32 scores)
+ * Host errors: TV_ERR_ARG, TV_ERR_SHAPE, TV_ERR_WORKSPACE.
+ * Device errors: TV_ERR_SELECTION (n4 < n_sel), TV_ERR_CAPACITY (n4 > c4_cap); that request's
+ * sel row is set to -1.
+ */
+size_t tv_indexer_workspace_size(const tv_shape* shape);
+int tv_indexer_topk(const tv_shape* shape, int d_idx, const void* q_idx, const void* k_idx,
+                    const int32_t* L, int32_t* sel, void* workspace, size_t ws_bytes,
+                    int32_t* status, tv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

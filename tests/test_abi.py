@@ -96,3 +96,15 @@ def test_workspace_size_grows_with_batch(lib):
     a = lib.tv_workspace_size(ctypes.byref(_shape(B=2)))
     b = lib.tv_workspace_size(ctypes.byref(_shape(B=4)))
     assert 0 < a < b and a % 256 == 0
+
+
+def test_indexer_validation(lib):
+    s = _shape(n_sel=64)
+    rc = lib.tv_indexer_topk(ctypes.byref(s), 12, None, None, None, None, None, 0, None, None)
+    assert rc == -2                                           # d_idx not a multiple of 8
+    s0 = _shape(n_sel=0)
+    rc = lib.tv_indexer_topk(ctypes.byref(s0), 64, None, None, None, None, None, 0, None, None)
+    assert rc == -1                                           # no selection size
+    rc = lib.tv_indexer_topk(ctypes.byref(s), 64, None, None, None, None, None, 0, None, None)
+    assert rc == -1                                           # null inputs
+    assert lib.tv_indexer_workspace_size(ctypes.byref(s)) == 2304         # 2 x 260 x 4, to 256

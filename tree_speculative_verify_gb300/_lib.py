@@ -31,6 +31,7 @@ EXPORTS = (
     "tv_attn_kernel_for",
     "tv_build_ancestor_mask", "tv_prefill_compress", "tv_branch_compress",
     "tv_tree_verify_attn", "tv_accept_walk", "tv_refresh_commit", "tv_tree_verify_attn_noalloc",
+    "tv_indexer_workspace_size", "tv_indexer_topk",
 )
 
 
@@ -70,6 +71,9 @@ _SIGS = {
                                     ctypes.c_int),
     "tv_accept_walk": ([_SHAPE] + [_P] * 7 + [_P], ctypes.c_int),
     "tv_refresh_commit": ([_SHAPE] + [_P] * 17 + [_P], ctypes.c_int),
+    "tv_indexer_workspace_size": ([_SHAPE], ctypes.c_size_t),
+    "tv_indexer_topk": ([_SHAPE, ctypes.c_int] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
+                        ctypes.c_int),
 }
 
 
@@ -199,3 +203,15 @@ def tv_refresh_commit(shape, accept_len, path, treeK, treeV, scrK4, scrV4, scrK1
                                   _p(rawK), _p(rawV), _p(c4K), _p(c4V), _p(c128K), _p(c128V),
                                   _p(L), _p(committed_pos), _p(status), _stream(stream))
     _check("tv_refresh_commit", rc)
+
+
+def tv_indexer_workspace_size(shape):
+    return int(load().tv_indexer_workspace_size(ctypes.byref(shape)))
+
+
+def tv_indexer_topk(shape, d_idx, q_idx, k_idx, L, sel, workspace, status, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().tv_indexer_topk(ctypes.byref(shape), ctypes.c_int(d_idx), _p(q_idx), _p(k_idx),
+                                _p(L), _p(sel), _p(workspace), ctypes.c_size_t(ws_bytes),
+                                _p(status), _stream(stream))
+    _check("tv_indexer_topk", rc)

@@ -106,6 +106,10 @@ int tv_launch_refresh(const tv_shape* s, const int32_t* accept_len, const int32_
                       void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
                       int32_t* committed, int32_t* status, cudaStream_t stream);
 
+int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const void* k_idx,
+                      const int32_t* L, int32_t* sel, void* workspace, int32_t* status,
+                      cudaStream_t stream);
+
 // ---- split-KV geometry of the SIMT kernel -----------------------------------------------------
 struct SimtPlan {
   int n_chunks;
@@ -163,7 +167,7 @@ extern "C" int tv_attn_kernel_for(const tv_shape* s) {
   if (!use_tc(s)) return TV_ATTN_SIMT;
   if (!tc_supported(s))
     return tv_set_error(TV_ERR_DTYPE, "tv_attn_kernel_for: the tcgen05 kernel needs bf16, d = 512, D <= 8, "
-                        "n_sel = 0 and an sm_103 device");
+                        "and an sm_103 device");
   return TV_ATTN_TCGEN05;
 }
 
@@ -343,7 +347,7 @@ extern "C" int tv_tree_verify_attn(const tv_shape* s, const void* Q, const void*
   if (use_tc(s)) {
     if (!tc_supported(s))
       return tv_set_error(TV_ERR_DTYPE,
-                          "%s: the tcgen05 kernel needs bf16, d = 512, D <= 8, n_sel = 0 and an sm_103 device", fn);
+                          "%s: the tcgen05 kernel needs bf16, d = 512, D <= 8 and an sm_103 device", fn);
     auto p = make_params<__nv_bfloat16>(s, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L, treeK,
                                         treeV, anc, raw_lo, scr_vis4, scr_vis128, scrK4, scrV4,
                                         scrK128, scrV128, scale, O, lse, status);
@@ -417,5 +421,41 @@ extern "C" int tv_refresh_commit(const tv_shape* s, const int32_t* accept_len,
   }
   return tv_launch_refresh(s, accept_len, path, treeK, treeV, scrK4, scrV4, scrK128, scrV128,
                            rawK, rawV, c4K, c4V, c128K, c128V, L, committed_pos, status,
+                           (cudaStream_t)stream);
+}
+
+// ---- indexer top-k ------------------------------------------------------------------------------
+static size_t indexer_ws(const tv_shape* s) {
+  return ((size_t)s->B * (size_t)s->c4_cap * sizeof(float) + 255) / 256 * 256;
+}
+
+extern "C" size_t tv_indexer_workspace_size(const tv_shape* s) {
+  if (check_shape(s, "tv_indexer_workspace_size") != TV_OK || s->B == 0) return 0;
+  return indexer_ws(s);
+}
+
+extern "C" int tv_indexer_topk(const tv_shape* s, int d_idx, const void* q_idx, const void* k_idx,
+                               const int32_t* L, int32_t* sel, void* workspace, size_t ws_bytes,
+                               int32_t* status, tv_stream_t stream) {
+  const char* fn = "tv_indexer_topk";
+  if (int rc = check_shape(s, fn)) return rc;
+  if (!has_c4(s) || s->n_sel <= 0)
+    return tv_set_error(TV_ERR_ARG, "%s: needs C4 in comp_mask and n_sel > 0 (n_sel = %d)", fn,
+                        s->n_sel);
+  if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0)
+    return tv_set_error(TV_ERR_SHAPE, "%s: d_idx = %d is not a multiple of 8 in 8..256", fn, d_idx);
+  if (s->B == 0) return TV_OK;
+  TV_REQUIRE(q_idx, fn);
+  TV_REQUIRE(k_idx, fn);
+  TV_REQUIRE(L, fn);
+  TV_REQUIRE(sel, fn);
+  TV_REQUIRE(status, fn);
+  if (((uintptr_t)q_idx | (uintptr_t)k_idx) & 15u)
+    return tv_set_error(TV_ERR_ARG, "%s: q_idx and k_idx must be 16-byte aligned", fn);
+  const size_t need = indexer_ws(s);
+  if (workspace == nullptr || ws_bytes < need)
+    return tv_set_error(TV_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes,
+                        need);
+  return tv_launch_indexer(s, d_idx, q_idx, k_idx, L, sel, workspace, status,
                            (cudaStream_t)stream);
 }

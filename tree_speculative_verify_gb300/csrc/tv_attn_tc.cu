@@ -77,6 +77,7 @@ struct Params {
   CUtensorMap mC4K, mC4V, mC128K, mC128V, mRawK, mRawV;
   CUtensorMap mTreeK, mTreeV, mS4K, mS4V, mS128K, mS128V;
   int B, D, H, DH, W, tail_mode, comp_mask, n_pairs, n_chunks;
+  int n_sel;       // > 0: the C4 maps point at the gathered selected entries, n_sel per request
   int tree_rows;   // B * D: the first row index past the tree / scratch tensors (zero fill)
   int64_t raw_cap, c4_cap, c128_cap;
   const int32_t* L;
@@ -104,14 +105,14 @@ __device__ __forceinline__ Layout layout_of(const Params& p, int b) {
   Layout y;
   const int L = p.L[b];
   const bool c4 = p.comp_mask & TV_COMP_C4, c128 = p.comp_mask & TV_COMP_C128;
-  const bool ok = L >= 0 && L <= p.raw_cap && (!c4 || L / 4 <= p.c4_cap) &&
-                  (!c128 || L / 128 <= p.c128_cap);
+  const int n4 = c4 ? (p.n_sel > 0 ? p.n_sel : L / 4) : 0;
+  const bool ok = L >= 0 && L <= p.raw_cap && n4 <= p.c4_cap && (!c128 || L / 128 <= p.c128_cap);
   if (!ok) {
     y.L = y.n4 = y.n128 = y.t0 = y.nraw = y.T4 = y.T128 = y.Traw = y.T = 0;
     return y;
   }
   y.L = L;
-  y.n4 = c4 ? L / 4 : 0;
+  y.n4 = n4;
   y.n128 = c128 ? L / 128 : 0;
   const int tail = p.tail_mode == TV_TAIL_WINDOW ? p.W : m_min_of(p.comp_mask) - 1;
   y.t0 = L - tail > 0 ? L - tail : 0;
@@ -158,6 +159,32 @@ __global__ void order_kernel(Params p, int32_t* order) {
     int rank = 0;
     for (int j = 0; j < p.B; ++j) rank += (tiles[j] > tb || (tiles[j] == tb && j < b)) ? 1 : 0;
     order[rank] = b;
+  }
+}
+
+// Selected C4 entries ("sparse" prefix attention): copies entry sel[b][i] of request b's K and V
+// into row i of a dense per-request buffer, so the attention kernel reads the selection as
+// contiguous tiles.  One warp per selected entry; an index outside 0 .. L/4 - 1 (or past the C4
+// capacity) records TV_ERR_SELECTION and leaves a zero row.
+__global__ void gather_sel_kernel(int B, int n_sel, int64_t c4_cap, const int32_t* __restrict__ L,
+                                  const int32_t* __restrict__ sel, const uint4* __restrict__ c4K,
+                                  const uint4* __restrict__ c4V, uint4* __restrict__ gK,
+                                  uint4* __restrict__ gV, int32_t* status) {
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= (int64_t)B * n_sel) return;
+  const int b = (int)(w / n_sel);
+  const int j = sel[w];
+  const int Lb = L[b];
+  const bool ok = Lb >= 0 && j >= 0 && j < Lb / 4 && j < c4_cap;
+  if (!ok && lane == 0) record_error(status, TV_ERR_SELECTION);
+  constexpr int kRowU4 = 512 * 2 / 16;   // 64 x 16 B per bf16 row of 512
+  const int64_t src = ((int64_t)b * c4_cap + (ok ? j : 0)) * kRowU4;
+  const int64_t dst = w * kRowU4;
+  for (int i = lane; i < kRowU4; i += 32) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    gK[dst + i] = ok ? c4K[src + i] : z;
+    gV[dst + i] = ok ? c4V[src + i] : z;
   }
 }
 
@@ -741,25 +768,45 @@ bool make_map(CUtensorMap* m, const void* base, int rank, uint64_t rows, uint64_
 
 int n_pairs_of(const tv_shape* s) { return ((s->D * s->H + 127) / 128 + 1) / 2; }
 
+// Number of KV chunks per request.  Clusters of 2 CTAs run one per SM pair; a cluster costs about
+// (its tiles + 2) tile-times (the Q load and the epilogue).  With T the largest tile count the
+// capacities allow, pick the chunk count that minimises waves x (ceil(T / n) + 2); a larger count
+// must win by more than 10 % (splitting adds fp32 partials and a merge pass).
 int tc_chunks(const tv_shape* s) {
-  const int64_t ctas = (int64_t)s->B * n_pairs_of(s) * 4;
+  static int pair_slots = 0;
+  if (pair_slots == 0) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 2)
+      sms = 152;
+    cudaGetLastError();
+    pair_slots = sms / 2;
+  }
   int64_t max_tiles = 1 + (s->tail_mode == TV_TAIL_WINDOW ? (s->W + 127) / 128 : 1);
-  if (s->comp_mask & TV_COMP_C4) max_tiles += (s->c4_cap + 127) / 128;
+  if (s->comp_mask & TV_COMP_C4) max_tiles += ((s->n_sel > 0 ? s->n_sel : s->c4_cap) + 127) / 128;
   if (s->comp_mask & TV_COMP_C128) max_tiles += (s->c128_cap + 127) / 128;
-  int64_t n = ctas >= 2 * 152 ? 1 : (2 * 152 + ctas - 1) / ctas;
-  if (n > max_tiles) n = max_tiles;
-  if (n < 1) n = 1;
-  if (n > 64) n = 64;
-  return (int)n;
+  const int64_t clusters1 = (int64_t)s->B * n_pairs_of(s) * 2;   // two value halves
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int n = 1; n <= 64 && n <= max_tiles; ++n) {
+    const int64_t waves = (clusters1 * n + pair_slots - 1) / pair_slots;
+    const int64_t cost = waves * ((max_tiles + n - 1) / n + 2);
+    if (best_cost < 0 || 10 * cost < 9 * best_cost) {
+      best_cost = cost;
+      best = n;
+    }
+  }
+  return best;
 }
 
 }  // namespace
 
 bool tv_tc_shape_ok(const tv_shape* s) {
-  return s->dtype == TV_BF16 && s->d == 512 && s->D <= tv::tc::kDp && s->n_sel == 0 &&
+  return s->dtype == TV_BF16 && s->d == 512 && s->D <= tv::tc::kDp &&
          s->B <= 12288 &&   // the ranking kernel keeps one int per request in shared memory
          (int64_t)s->B * s->raw_cap < ((int64_t)1 << 31) &&
          (int64_t)s->B * s->c4_cap < ((int64_t)1 << 31) &&
+         (int64_t)s->B * s->n_sel < ((int64_t)1 << 31) &&
          (int64_t)s->B * s->c128_cap < ((int64_t)1 << 31);
 }
 
@@ -777,12 +824,16 @@ bool tv_tc_available() {
   return cached == 1;
 }
 
-// Workspace: the request order (B int32, padded to 256 B), then the split-KV partials.
+// Workspace: the request order (B int32, padded to 256 B), the gathered selected C4 entries (K
+// then V, B x n_sel x 512 bf16 each, when n_sel > 0), then the split-KV partials.
 static size_t order_bytes(const tv_shape* s) { return ((size_t)s->B * 4 + 255) / 256 * 256; }
+static size_t gather_bytes(const tv_shape* s) {
+  return s->n_sel > 0 ? (size_t)s->B * s->n_sel * 512 * 2 : 0;   // one of K / V (multiple of 1 KB)
+}
 
 size_t tv_tc_workspace_size(const tv_shape* s) {
   const int n = tc_chunks(s);
-  size_t bytes = order_bytes(s);
+  size_t bytes = order_bytes(s) + 2 * gather_bytes(s);
   if (n > 1) bytes += (size_t)s->B * s->D * s->H * n * (s->d + 4) * sizeof(float);
   return bytes;
 }
@@ -795,8 +846,14 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   const uint64_t B = (uint64_t)s->B;
   // an inactive compressor's maps are pointed at the raw buffer (never read: its tiles are empty)
   const bool c4 = s->comp_mask & TV_COMP_C4, c128 = s->comp_mask & TV_COMP_C128;
+  char* ws = reinterpret_cast<char*>(workspace);
   const void* c4K = c4 ? a.c4K : a.rawK;
   const void* c4V = c4 ? a.c4V : a.rawV;
+  const bool gathered = c4 && s->n_sel > 0;
+  if (gathered) {
+    c4K = ws + order_bytes(s);
+    c4V = ws + order_bytes(s) + gather_bytes(s);
+  }
   const void* c128K = c128 ? a.c128K : a.rawK;
   const void* c128V = c128 ? a.c128V : a.rawV;
   const void* s4K = c4 ? a.scrK4 : a.treeK;
@@ -804,7 +861,8 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   const void* s128K = c128 ? a.scrK128 : a.treeK;
   const void* s128V = c128 ? a.scrV128 : a.treeV;
   auto rows_or_one = [](uint64_t r) { return r > 0 ? r : (uint64_t)1; };
-  const uint64_t c4rows = rows_or_one(B * (uint64_t)(c4 ? s->c4_cap : s->raw_cap));
+  const uint64_t c4rows =
+      rows_or_one(B * (uint64_t)(gathered ? s->n_sel : c4 ? s->c4_cap : s->raw_cap));
   const uint64_t c128rows = rows_or_one(B * (uint64_t)(c128 ? s->c128_cap : s->raw_cap));
   const uint64_t rawrows = rows_or_one(B * (uint64_t)s->raw_cap);
   const uint64_t trows = B * (uint64_t)s->D;
@@ -831,7 +889,8 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.n_chunks = tc_chunks(s);
   p.tree_rows = (int)trows;
   p.raw_cap = s->raw_cap;
-  p.c4_cap = s->c4_cap;
+  p.c4_cap = gathered ? s->n_sel : s->c4_cap;
+  p.n_sel = gathered ? s->n_sel : 0;
   p.c128_cap = s->c128_cap;
   p.L = a.L;
   p.raw_lo = a.raw_lo;
@@ -843,8 +902,16 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.lse = a.lse;
   int32_t* order = reinterpret_cast<int32_t*>(workspace);
   p.order = order;
-  p.part = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + order_bytes(s));
+  p.part = reinterpret_cast<float*>(ws + order_bytes(s) + 2 * gather_bytes(s));
   p.status = a.status;
+  if (gathered && s->B > 0) {
+    const int64_t rows = (int64_t)s->B * s->n_sel;
+    gather_sel_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        s->B, s->n_sel, s->c4_cap, a.L, a.sel, reinterpret_cast<const uint4*>(a.c4K),
+        reinterpret_cast<const uint4*>(a.c4V), reinterpret_cast<uint4*>(ws + order_bytes(s)),
+        reinterpret_cast<uint4*>(ws + order_bytes(s) + gather_bytes(s)), a.status);
+    if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 selection gather)")) return rc;
+  }
   // one CTA ranks all requests (B <= 12288 fits its default shared memory)
   order_kernel<<<1, 1024, (size_t)s->B * sizeof(int), stream>>>(p, order);
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;

@@ -3,8 +3,8 @@
 
 #include "tv_attn_common.cuh"
 
-// True when the tensor-core kernel takes this shape (bf16, d = 512, D <= 8, no selection list,
-// B <= 12288).
+// True when the tensor-core kernel takes this shape (bf16, d = 512, D <= 8, B <= 12288; a C4
+// selection list is gathered into the workspace first).
 bool tv_tc_shape_ok(const tv_shape* s);
 // True when the tensor-core kernel is compiled in and the current device can run it.
 bool tv_tc_available();

@@ -1,0 +1,196 @@
+// Indexer top-k: the selected C4 entries of the sparse prefix attention, chosen on the device.
+//
+// "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for Efficient Inference" §2.2:
+// CSA is compressed *sparse* attention -- a query reads a selected subset of the compressed C4
+// entries.  The report gives no selection rule; the long-context workload's stand-in scores entry
+// j of request b as q_idx[b] . k_idx[b][j] (dimension d_idx) and keeps the n_sel best, equal
+// scores going to the lower index, listed in ascending order.
+//
+// Precision: the scores decide an integer selection, so the kernel fixes them exactly: bf16
+// inputs; each product rounded to fp32 (exact for bf16 operands) and added to the running fp32
+// sum in index order i = 0 .. d_idx-1 with one round-to-nearest-even per addition and no fused
+// multiply-add (__fmul_rn / __fadd_rn).
+//
+// Two kernels:
+//   score_kernel   one thread per (request, entry): the fp32 score into the workspace.
+//   select_kernel  one 1024-thread CTA per request: an 8-bit-digit radix select (four passes over
+//                  the request's scores, shared-memory histograms) finds the n_sel-th largest key;
+//                  then every thread counts the entries above it and the ties in its contiguous
+//                  index range, two block-wide prefix sums place its kept entries, and it writes
+//                  them in ascending order (ties: the lowest indices).
+#include "tv_common.cuh"
+
+namespace tv {
+namespace {
+
+constexpr int kSelThreads = 1024;
+
+// Order-preserving map of an fp32 score to an unsigned key (larger score -> larger key); -0 and
+// +0 map to the same key.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void score_kernel(int B, int64_t c4_cap, int d_idx, const uint16_t* __restrict__ q_idx,
+                             const uint16_t* __restrict__ k_idx, const int32_t* __restrict__ L,
+                             float* __restrict__ score) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)B * c4_cap) return;
+  const int b = (int)(t / c4_cap);
+  const int64_t j = t - (int64_t)b * c4_cap;
+  const int Lb = L[b];
+  if (Lb < 0 || j >= Lb / 4) return;
+  const uint4* q = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx);
+  const uint4* k = reinterpret_cast<const uint4*>(k_idx + t * d_idx);
+  float s = 0.f;
+  for (int c = 0; c < d_idx / 8; ++c) {
+    const uint4 qa = q[c], ka = k[c];
+    const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {   // element 2h (low half) before 2h+1 (high half)
+      s = __fadd_rn(s, __fmul_rn(bf16_lo(qw[h]), bf16_lo(kw[h])));
+      s = __fadd_rn(s, __fmul_rn(bf16_hi(qw[h]), bf16_hi(kw[h])));
+    }
+  }
+  score[t] = s;
+}
+
+// Block-wide exclusive prefix sum of one int per thread (thread order); writes the block total to
+// *total.  `warp_tot` holds 33 ints of shared memory.
+__device__ __forceinline__ int block_exclusive_sum(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+    int z = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    warp_tot[lane] = z - w;
+    if (lane == 31) warp_tot[32] = z;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + x - v;
+  *total = warp_tot[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int n_sel,
+                                                             const int32_t* __restrict__ L,
+                                                             const float* __restrict__ score,
+                                                             int32_t* __restrict__ sel,
+                                                             int32_t* status) {
+  __shared__ unsigned hist[256];
+  __shared__ int warp_tot[33];
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_krem;
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int Lb = L[b];
+  const int64_t n4 = Lb >= 0 ? Lb / 4 : -1;
+  int32_t* out = sel + (int64_t)b * n_sel;
+  if (n4 < n_sel || n4 > c4_cap) {
+    if (threadIdx.x == 0) record_error(status, n4 > c4_cap ? TV_ERR_CAPACITY : TV_ERR_SELECTION);
+    for (int i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = -1;
+    return;
+  }
+  const float* sc = score + (int64_t)b * c4_cap;
+  if (threadIdx.x == 0) {
+    s_prefix = 0u;
+    s_mask = 0u;
+    s_krem = n_sel;
+  }
+  __syncthreads();
+  // radix select of the n_sel-th largest key, most significant digit first.  Scores of one request
+  // share few exponents, so lanes of a warp that hit the same bin are merged before the atomic.
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
+    for (int64_t j0 = 0; j0 < n4; j0 += blockDim.x) {
+      const int64_t j = j0 + threadIdx.x;
+      int bin = -1;
+      if (j < n4) {
+        const uint32_t key = score_key(sc[j]);
+        if ((key & mask) == prefix) bin = (int)((key >> shift) & 255u);
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int krem = s_krem;
+      int above = 0;
+      int digit = 0;
+      for (int d = 255; d >= 0; --d) {
+        const int c = (int)hist[d];
+        if (above + c >= krem) {
+          digit = d;
+          break;
+        }
+        above += c;
+      }
+      s_krem = krem - above;
+      s_prefix = prefix | ((uint32_t)digit << shift);
+      s_mask = mask | (255u << shift);
+    }
+    __syncthreads();
+  }
+  const uint32_t T = s_prefix;   // key of the n_sel-th best entry
+  const int need_eq = s_krem;    // entries with key == T to keep: the lowest-indexed ones
+  // thread t owns the contiguous index range [t * per, (t + 1) * per): count, scan, then write its
+  // kept entries in ascending order at their final positions
+  const int64_t per = (n4 + blockDim.x - 1) / blockDim.x;
+  const int64_t lo = threadIdx.x * per, hi = lo + per < n4 ? lo + per : n4;
+  int gt = 0, eq = 0;
+  for (int64_t j = lo; j < hi; ++j) {
+    const uint32_t key = score_key(sc[j]);
+    gt += key > T;
+    eq += key == T;
+  }
+  int gt_total, eq_total;
+  const int gt_before = block_exclusive_sum(gt, warp_tot, &gt_total);
+  const int eq_before = block_exclusive_sum(eq, warp_tot, &eq_total);
+  int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+  int eq_rank = eq_before;
+  for (int64_t j = lo; j < hi; ++j) {
+    const uint32_t key = score_key(sc[j]);
+    bool take = key > T;
+    if (key == T) take = eq_rank++ < need_eq;
+    if (take) out[pos++] = (int32_t)j;
+  }
+}
+
+}  // namespace
+}  // namespace tv
+
+int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const void* k_idx,
+                      const int32_t* L, int32_t* sel, void* workspace, int32_t* status,
+                      cudaStream_t stream) {
+  float* score = reinterpret_cast<float*>(workspace);
+  const int64_t n = (int64_t)s->B * s->c4_cap;
+  if (n > 0) {
+    tv::score_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
+        s->B, s->c4_cap, d_idx, reinterpret_cast<const uint16_t*>(q_idx),
+        reinterpret_cast<const uint16_t*>(k_idx), L, score);
+    if (int rc = tv_check_launch("tv_indexer_topk (scores)")) return rc;
+  }
+  tv::select_kernel<<<s->B, tv::kSelThreads, 0, stream>>>(s->c4_cap, s->n_sel, L, score, sel,
+                                                          status);
+  return tv_check_launch("tv_indexer_topk (select)");
+}

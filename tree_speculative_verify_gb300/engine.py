@@ -40,10 +40,12 @@ class DeviceState:
     c128K: torch.Tensor
     c128V: torch.Tensor
     L: torch.Tensor
+    k_idx: torch.Tensor = None    # [B][c4_cap][64] bf16 indexer keys (sparse C4 path only)
 
     def clone(self):
         return DeviceState(*(t.clone() for t in (self.rawK, self.rawV, self.c4K, self.c4V,
-                                                 self.c128K, self.c128V, self.L)))
+                                                 self.c128K, self.c128V, self.L)),
+                           k_idx=self.k_idx)
 
 
 @dataclass
@@ -74,6 +76,8 @@ class RoundBuffers:
     committed: torch.Tensor
     status: torch.Tensor
     workspace: torch.Tensor
+    q_idx: torch.Tensor = None    # [B][64] bf16 indexer queries (sparse C4 path only)
+    idx_ws: torch.Tensor = None   # indexer score workspace
 
 
 def alloc_state(wl, device="cuda"):
@@ -84,7 +88,8 @@ def alloc_state(wl, device="cuda"):
         rawK=wl.rawK.to(device), rawV=wl.rawV.to(device),
         c4K=z(wl.cap4 if 4 in wl.ms else 0), c4V=z(wl.cap4 if 4 in wl.ms else 0),
         c128K=z(wl.cap128 if 128 in wl.ms else 0), c128V=z(wl.cap128 if 128 in wl.ms else 0),
-        L=torch.as_tensor(wl.L, dtype=torch.int32).to(device))
+        L=torch.as_tensor(wl.L, dtype=torch.int32).to(device),
+        k_idx=None if wl.k_idx is None else wl.k_idx.to(device))
 
 
 def alloc_round(wl, shape, device="cuda"):
@@ -114,12 +119,20 @@ def alloc_round(wl, shape, device="cuda"):
         accept_len=torch.zeros(B, **i32), path=torch.zeros((B, D), **i32),
         bonus=torch.zeros(B, **i32), committed=torch.zeros((B, D), **i32),
         status=torch.zeros(1, **i32),
-        workspace=torch.empty(max(ws, 256), dtype=torch.uint8, device=device))
+        workspace=torch.empty(max(ws, 256), dtype=torch.uint8, device=device),
+        q_idx=None if wl.q_idx is None else wl.q_idx.to(device),
+        idx_ws=None if wl.q_idx is None else torch.empty(
+            max(_lib.tv_indexer_workspace_size(shape), 256), dtype=torch.uint8, device=device))
 
 
 def prefill(shape, st, rb, stream=None):
     _lib.tv_prefill_compress(shape, st.rawK, st.rawV, st.L, rb.g4, rb.g128, st.c4K, st.c4V,
                              st.c128K, st.c128V, rb.status, stream)
+
+
+def indexer(shape, st, rb, stream=None):
+    """Device selection of the n_sel C4 entries per request into ``rb.sel`` (sparse path)."""
+    _lib.tv_indexer_topk(shape, 64, rb.q_idx, st.k_idx, st.L, rb.sel, rb.idx_ws, rb.status, stream)
 
 
 def plan(shape, st, rb, stream=None):
@@ -152,8 +165,11 @@ def refresh(shape, st, rb, stream=None):
                            st.c128V, st.L, rb.committed, rb.status, stream)
 
 
-def verify_round(shape, st, rb, scale=None, stream=None, commit=True):
-    """One target-verify round: plan, scratch pad, attention, acceptance, refresh."""
+def verify_round(shape, st, rb, scale=None, stream=None, commit=True, select=False):
+    """One target-verify round: plan, scratch pad, attention, acceptance, refresh; with
+    ``select`` the indexer first picks the sparse path's C4 entries on the device."""
+    if select:
+        indexer(shape, st, rb, stream)
     plan(shape, st, rb, stream)
     branch_compress(shape, st, rb, stream)
     attention(shape, st, rb, scale, stream)
@@ -172,16 +188,16 @@ class RoundGraph:
     must stay allocated and at the same addresses; their contents may change between replays.
     """
 
-    def __init__(self, shape, st, rb, scale=None, commit=True, prologue=None):
+    def __init__(self, shape, st, rb, scale=None, commit=True, prologue=None, select=False):
         # one eager round first: per-device set-up of the library happens outside the capture
-        verify_round(shape, st, rb, scale, None, commit)
+        verify_round(shape, st, rb, scale, None, commit, select)
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
             stream = torch.cuda.current_stream()
             if prologue is not None:
                 prologue()
-            verify_round(shape, st, rb, scale, stream, commit)
+            verify_round(shape, st, rb, scale, stream, commit, select)
 
     def replay(self):
         self.graph.replay()

@@ -57,6 +57,8 @@ class Workload:
     treeV: torch.Tensor
     g: dict                 # {m: float32 tensor [d]}
     sel: np.ndarray = None  # [B, n_sel] sorted selected C4 indices, or None
+    q_idx: torch.Tensor = None   # [B, 64] bf16 indexer queries (with a selection list)
+    k_idx: torch.Tensor = None   # [B, cap4, 64] bf16 indexer keys of the C4 entries
     p_match: float = 0.0
     meta: dict = field(default_factory=dict)
 
@@ -176,22 +178,27 @@ def make_workload(name, *, B, D, H, d, W, tail_mode, ms, dtype, L, k, steps, p_m
     treeV = _store(kv_scale * rng.standard_normal((B, D, d)), dtype)
     g = {m: torch.from_numpy(rng.standard_normal(d).astype(np.float32)) for m in (4, 128)}
     g = {m: g[m] for m in ms}
-    sel = None
+    sel = q_idx = k_idx = None
     if n_sel:
-        # indexer stand-in: score q_idx . k_idx (dim 64) per C4 entry from the root query's
-        # indexer projection, keep the n_sel best (ties to the lower index), sorted ascending.
+        # indexer inputs: a bf16 query (dim 64) per request from the root and a bf16 key per C4
+        # entry; rows past a request's L // 4 entries are zero.  The selection list handed to the
+        # attention tests is the stand-in of the long-context workload: the n_sel best fp64
+        # scores q_idx . k_idx (ties to the lower index), sorted ascending.
         sel = np.empty((B, n_sel), dtype=np.int32)
+        q_idx = torch.zeros((B, 64), dtype=torch.bfloat16)
+        k_idx = torch.zeros((B, cap4, 64), dtype=torch.bfloat16)
         for b in range(B):
             n4 = int(Ls[b]) // 4
-            q_idx = rng.standard_normal(64)
-            k_idx = rng.standard_normal((n4, 64))
-            score = k_idx @ q_idx
+            q_idx[b] = _store(rng.standard_normal(64), "bf16")
+            k_idx[b, :n4] = _store(rng.standard_normal((n4, 64)), "bf16")
+            score = k_idx[b, :n4].double().numpy() @ q_idx[b].double().numpy()
             order = np.lexsort((np.arange(n4), -score))
             sel[b] = np.sort(order[:n_sel])
     return Workload(name=name, B=B, D=D, H=H, d=d, W=W, tail_mode=tail_mode, ms=tuple(ms),
                     dtype=dtype, L=Ls, raw_cap=raw_cap, cap4=cap4, cap128=cap128,
                     parents=parents, draft=draft, target=target, Q=Q, rawK=rawK, rawV=rawV,
-                    treeK=treeK, treeV=treeV, g=g, sel=sel, p_match=p_match,
+                    treeK=treeK, treeV=treeV, g=g, sel=sel, q_idx=q_idx, k_idx=k_idx,
+                    p_match=p_match,
                     meta=dict(seed=seed, k=k, steps=steps, kv_scale=kv_scale, L_spec=L))
 
 
