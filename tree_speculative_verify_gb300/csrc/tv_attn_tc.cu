@@ -35,8 +35,8 @@
 //               from TMEM, mask, online softmax with a lazily updated row maximum, write P_t back
 //               into the S columns as packed bf16, rescale O in TMEM when the maximum grows by
 //               more than 2^8, and finally write O.
-//   warp 10     lane 0: once every softmax warp of the CTA has stored P_t, arrives on the
-//               leader's p_full (a cluster-scope release that stalls its thread for a while).
+//   warp 10     lane 0: once every softmax warp of the CTA has stored P_t, signals the leader's
+//               p_full (leader: local arrive with expect_tx; follower: a 4-byte st.async).
 // TMEM columns: S/P double buffer at [0,128) and [128,256), O at [256,512).
 // Every mbarrier wait is bounded; on timeout the CTA records TV_ERR_TIMEOUT, stops issuing work,
 // drains its own copies and MMAs (bounded) and frees its TMEM.
@@ -195,7 +195,9 @@ struct __align__(1024) Smem {
   uint64_t empty[kSlots];      // the pair's MMAs are done with the slot
   uint64_t q_full;
   uint64_t s_full[2];
-  uint64_t p_full[2];          // (leader) P written by both CTAs' softmax warps
+  uint64_t p_full[2];          // (leader) P written by both CTAs' softmax warps: the leader's
+                               // arrive with expect_tx(4) + the follower's 4-byte st.async
+  uint32_t p_flag[2];          // (leader) landing word of the follower's st.async
   uint64_t p_local[2];         // this CTA's softmax warps have written P (one arrive per warp)
   uint64_t pv_done;
   uint64_t o_full;
@@ -431,19 +433,26 @@ __device__ __forceinline__ void pair_sync(int quad) {
 }
 
 // ---- signal warp: P of tile i is in both CTAs' TMEM -> the leader's MMA issuer ----------------
-// Lane 0 waits until all softmax warps of this CTA have stored P_i (local barrier), then performs
-// the release-arrive at cluster scope on the leader's p_full.  That remote arrive stalls its
-// thread for several hundred nanoseconds, which would otherwise delay the next tile's softmax.
-__device__ void p_signal(const Params& p, Smem& sm, int n) {
-  const uint32_t p_full_leader[2] = {mapa_cluster(smem_u32(&sm.p_full[0]), 0),
-                                     mapa_cluster(smem_u32(&sm.p_full[1]), 0)};
+// Lane 0 waits until all softmax warps of this CTA have stored P_i (local barrier).  The leader
+// then arrives on its own p_full with expect_tx(4); the follower completes those 4 bytes with an
+// asynchronous 4-byte store into the leader's shared memory (st.async with complete_tx), which
+// lands much sooner than a cluster-scope release-arrive.  The follower cannot signal tile i + 2
+// before p_full(i) completed: its S(i+2) needs the leader's PV(i), issued after p_full(i).
+__device__ void p_signal(const Params& p, Smem& sm, int n, uint32_t rank) {
+  const uint32_t flag_leader[2] = {mapa_cluster(smem_u32(&sm.p_flag[0]), 0),
+                                   mapa_cluster(smem_u32(&sm.p_flag[1]), 0)};
+  const uint32_t bar_leader[2] = {mapa_cluster(smem_u32(&sm.p_full[0]), 0),
+                                  mapa_cluster(smem_u32(&sm.p_full[1]), 0)};
   for (int i = 0; i < n; ++i) {
     const int sb = i & 1;
     if (!mbar_wait(&sm.p_local[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs)) {
       fail(sm, p.status);
       return;
     }
-    mbar_arrive_cluster(p_full_leader[sb]);
+    if (rank == 0)
+      mbar_arrive_expect_tx(&sm.p_full[sb], 4);
+    else
+      st_async_signal(flag_leader[sb], (uint32_t)i, bar_leader[sb]);
   }
 }
 
@@ -685,8 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.s_full[0], 1);
     mbar_init(&sm.s_full[1], 1);
-    mbar_init(&sm.p_full[0], 2);
-    mbar_init(&sm.p_full[1], 2);
+    mbar_init(&sm.p_full[0], 1);
+    mbar_init(&sm.p_full[1], 1);
     mbar_init(&sm.p_local[0], kSmxWarps);
     mbar_init(&sm.p_local[1], kSmxWarps);
     mbar_init(&sm.pv_done, 1);
@@ -717,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       }
       __syncwarp();
     } else if (warp == kSigWarp) {
-      if (lane == 0) p_signal(p, sm, te - tb);
+      if (lane == 0) p_signal(p, sm, te - tb, rank);
       __syncwarp();
     } else {
       softmax_epilogue(p, sm, b, rt, half, chunk, y, tb, te);

@@ -18,12 +18,17 @@
 //                  then every thread counts the entries above it and the ties in its contiguous
 //                  index range, two block-wide prefix sums place its kept entries, and it writes
 //                  them in ascending order (ties: the lowest indices).
+#include <mutex>
+
 #include "tv_common.cuh"
 
 namespace tv {
 namespace {
 
 constexpr int kSelThreads = 1024;
+// Keys staged in shared memory when a request has at most this many C4 entries (160 KB): the four
+// radix passes and the final pass then read shared memory instead of re-reading the scores.
+constexpr int kSmemKeys = 40960;
 
 // Order-preserving map of an fp32 score to an unsigned key (larger score -> larger key); -0 and
 // +0 map to the same key.
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
                                                              const float* __restrict__ score,
                                                              int32_t* __restrict__ sel,
                                                              int32_t* status) {
+  extern __shared__ uint32_t keys_smem[];
   __shared__ unsigned hist[256];
   __shared__ int warp_tot[33];
   __shared__ uint32_t s_prefix, s_mask;
@@ -110,6 +116,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
     return;
   }
   const float* sc = score + (int64_t)b * c4_cap;
+  const bool staged = n4 <= kSmemKeys;
+  if (staged) {
+#pragma unroll 8
+    for (int64_t j = threadIdx.x; j < n4; j += blockDim.x) keys_smem[j] = score_key(sc[j]);
+  }
+  auto key_at = [&](int64_t j) -> uint32_t { return staged ? keys_smem[j] : score_key(sc[j]); };
   if (threadIdx.x == 0) {
     s_prefix = 0u;
     s_mask = 0u;
@@ -126,7 +138,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
       const int64_t j = j0 + threadIdx.x;
       int bin = -1;
       if (j < n4) {
-        const uint32_t key = score_key(sc[j]);
+        const uint32_t key = key_at(j);
         if ((key & mask) == prefix) bin = (int)((key >> shift) & 255u);
       }
       const unsigned peers = __match_any_sync(0xffffffffu, bin);
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
   const int64_t lo = threadIdx.x * per, hi = lo + per < n4 ? lo + per : n4;
   int gt = 0, eq = 0;
   for (int64_t j = lo; j < hi; ++j) {
-    const uint32_t key = score_key(sc[j]);
+    const uint32_t key = key_at(j);
     gt += key > T;
     eq += key == T;
   }
@@ -169,7 +181,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
   int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
   int eq_rank = eq_before;
   for (int64_t j = lo; j < hi; ++j) {
-    const uint32_t key = score_key(sc[j]);
+    const uint32_t key = key_at(j);
     bool take = key > T;
     if (key == T) take = eq_rank++ < need_eq;
     if (take) out[pos++] = (int32_t)j;
@@ -190,7 +202,26 @@ int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const voi
         reinterpret_cast<const uint16_t*>(k_idx), L, score);
     if (int rc = tv_check_launch("tv_indexer_topk (scores)")) return rc;
   }
-  tv::select_kernel<<<s->B, tv::kSelThreads, 0, stream>>>(s->c4_cap, s->n_sel, L, score, sel,
-                                                          status);
+  // shared memory for the staged keys, sized by the capacity (requests with more entries than
+  // kSmemKeys read the scores from global memory instead)
+  const int64_t staged = s->c4_cap < tv::kSmemKeys ? s->c4_cap : tv::kSmemKeys;
+  const size_t smem = (size_t)staged * sizeof(uint32_t);
+  // once per device (a plain host call that also stays out of any stream being captured)
+  static std::mutex attr_mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return tv_check_launch("tv_indexer_topk (device query)");
+  {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(tv::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(tv::kSmemKeys * sizeof(uint32_t))) != cudaSuccess)
+        return tv_check_launch("tv_indexer_topk (shared-memory attribute)");
+      attr_set[dev] = true;
+    }
+  }
+  tv::select_kernel<<<s->B, tv::kSelThreads, smem, stream>>>(s->c4_cap, s->n_sel, L, score, sel,
+                                                             status);
   return tv_check_launch("tv_indexer_topk (select)");
 }

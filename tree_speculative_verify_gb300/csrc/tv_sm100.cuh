@@ -143,6 +143,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// 4-byte asynchronous store into a peer CTA's shared memory that signals the peer's mbarrier with
+// complete_tx(4) when it lands (both addresses are shared::cluster addresses of the peer).
+__device__ __forceinline__ void st_async_signal(uint32_t cluster_addr, uint32_t value,
+                                                uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(value), "r"(cluster_bar)
+      : "memory");
+}
 
 // Bring a box of a tensor into L2 ahead of time (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
