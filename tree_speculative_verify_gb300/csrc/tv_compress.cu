@@ -47,6 +47,26 @@ struct Vec<float, 4> {
     out[3] = f.w;
   }
 };
+// Raw 16-byte vector and its conversion to fp32 (loads are issued first, converted later, so
+// many loads are in flight at once).
+template <typename T>
+__device__ __forceinline__ uint4 ld16(const T* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void cvt16(uint4 u, __nv_bfloat16*, float* out) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(h[k]);
+    out[2 * k] = f.x;
+    out[2 * k + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void cvt16(uint4 u, float*, float* out) {
+  out[0] = __uint_as_float(u.x);
+  out[1] = __uint_as_float(u.y);
+  out[2] = __uint_as_float(u.z);
+  out[3] = __uint_as_float(u.w);
+}
+
 template <typename T>
 struct VecWidth;
 template <>
@@ -72,19 +92,45 @@ __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int 
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  // 1. gate logits z_t = K_t . g: warp per token, lanes over 16-byte vectors of the row
-#pragma unroll 4
-  for (int t = warp; t < m; t += nwarps) {
-    const T* k = rowK[t];
-    float acc = 0.f;
-    for (int i = lane * VW; i < d; i += 32 * VW) {
-      float kv[VW];
-      Vec<T, VW>::load(k + i, kv);
+  // 1. gate logits z_t = K_t . g: warp per token (token t on warp t % nwarps), lanes over 16-byte
+  //    vectors of the row (lane l: dims l*VW + 32*VW*k); each warp loads a batch of its tokens
+  //    before using any, and keeps its slice of g in registers
+  constexpr int KVMAX = 512 / (32 * VW);   // vectors per lane at the largest head dim
+  constexpr int U1 = 8 / KVMAX;            // tokens per batch
+  float gr[KVMAX][VW];
 #pragma unroll
-      for (int e = 0; e < VW; ++e) acc = fmaf(kv[e], g[i + e], acc);
+  for (int k = 0; k < KVMAX; ++k) {
+    const int i = lane * VW + 32 * VW * k;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) gr[k][e] = i < d ? g[i + e] : 0.f;
+  }
+  for (int t0 = warp; t0 < m; t0 += nwarps * U1) {
+    uint4 raw[U1][KVMAX];
+#pragma unroll
+    for (int u = 0; u < U1; ++u) {
+      const int t = t0 + u * nwarps;
+#pragma unroll
+      for (int k = 0; k < KVMAX; ++k) {
+        const int i = lane * VW + 32 * VW * k;
+        raw[u][k] = (t < m && i < d) ? ld16(rowK[t] + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) w_smem[t] = acc;
+#pragma unroll
+    for (int u = 0; u < U1; ++u) {
+      const int t = t0 + u * nwarps;
+      if (t >= m) break;   // warp-uniform
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < KVMAX; ++k) {
+        if (lane * VW + 32 * VW * k >= d) break;
+        float kv[VW];
+        cvt16(raw[u][k], (T*)nullptr, kv);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) acc = fmaf(kv[e], gr[k][e], acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) w_smem[t] = acc;
+    }
   }
   __syncthreads();
   // 2. softmax over the m logits
@@ -116,16 +162,28 @@ __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int 
     float ak[VW], av[VW];
 #pragma unroll
     for (int e = 0; e < VW; ++e) ak[e] = av[e] = 0.f;
-#pragma unroll 4
-    for (int t = gi; t < m; t += G) {
-      const float w = w_smem[t];
-      float kv[VW], vv[VW];
-      Vec<T, VW>::load(rowK[t] + i, kv);
-      Vec<T, VW>::load(rowV[t] + i, vv);
+    constexpr int U3 = 4;   // tokens whose K and V vectors are loaded before use
+    for (int t0 = gi; t0 < m; t0 += G * U3) {
+      uint4 rk[U3], rv[U3];
 #pragma unroll
-      for (int e = 0; e < VW; ++e) {
-        ak[e] = fmaf(w, kv[e], ak[e]);
-        av[e] = fmaf(w, vv[e], av[e]);
+      for (int u = 0; u < U3; ++u) {
+        const int t = t0 + u * G;
+        rk[u] = t < m ? ld16(rowK[t] + i) : make_uint4(0u, 0u, 0u, 0u);
+        rv[u] = t < m ? ld16(rowV[t] + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < U3; ++u) {
+        const int t = t0 + u * G;
+        if (t >= m) break;
+        const float w = w_smem[t];
+        float kv[VW], vv[VW];
+        cvt16(rk[u], (T*)nullptr, kv);
+        cvt16(rv[u], (T*)nullptr, vv);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) {
+          ak[e] = fmaf(w, kv[e], ak[e]);
+          av[e] = fmaf(w, vv[e], av[e]);
+        }
       }
     }
 #pragma unroll
@@ -149,7 +207,7 @@ __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int 
 // ---- prefill: every complete block of the committed prefix ---------------------------------
 // grid.x: entry index (strided), grid.y: request.
 template <typename T>
-__global__ void prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
+__global__ void __launch_bounds__(kCompressThreads, 2) prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
                                const T* __restrict__ rawK, const T* __restrict__ rawV,
                                const int32_t* __restrict__ L, const float* __restrict__ g,
                                T* __restrict__ CK, T* __restrict__ CV, int32_t* status) {
@@ -182,7 +240,7 @@ __global__ void prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
 // with the block that v's token closes (positions pos_v - m + 1 .. pos_v of prefix + path(v)) or
 // with zeros.
 template <typename T>
-__global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
+__global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
                               const T* __restrict__ rawK, const T* __restrict__ rawV,
                               const int32_t* __restrict__ L, const T* __restrict__ treeK,
                               const T* __restrict__ treeV, const int32_t* __restrict__ parents,
@@ -193,6 +251,7 @@ __global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
   __shared__ float w[128];
   __shared__ float red[2 * kRedFloats];
   __shared__ int path[kMaxD];   // path[k] = ancestor of v at depth k
+  __shared__ int s_par[kMaxD];
   __shared__ int s_depth;
   __shared__ int s_ok;
   const int v = blockIdx.x;
@@ -211,6 +270,9 @@ __global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
   const int Lb = L[b];
   const int32_t* par = parents + (int64_t)b * D;
 
+  // the request's parent array in one round trip; the chain walk then runs in shared memory
+  for (int u = threadIdx.x; u < D; u += blockDim.x) s_par[u] = par[u];
+  __syncthreads();
   if (threadIdx.x == 0) {
     int ok = (Lb >= 0 && Lb <= raw_cap) ? 1 : 0;
     int dep = 0;
@@ -219,12 +281,12 @@ __global__ void branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
     for (int step = 0; step < D && ok; ++step) {
       chain[dep] = u;
       if (u == 0) break;
-      const int p = par[u];
+      const int p = s_par[u];
       if (p < 0 || p >= u) { ok = 0; break; }
       u = p;
       ++dep;
     }
-    if (ok && par[0] != -1) ok = 0;
+    if (ok && s_par[0] != -1) ok = 0;
     if (ok) {
       for (int k = 0; k <= dep; ++k) path[k] = chain[dep - k];
     } else {

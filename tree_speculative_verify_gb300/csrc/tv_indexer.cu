@@ -15,9 +15,9 @@
 //   score_kernel   one thread per (request, entry): the fp32 score into the workspace.
 //   select_kernel  one 1024-thread CTA per request: an 8-bit-digit radix select (four passes over
 //                  the request's scores, shared-memory histograms) finds the n_sel-th largest key;
-//                  then every thread counts the entries above it and the ties in its contiguous
-//                  index range, two block-wide prefix sums place its kept entries, and it writes
-//                  them in ascending order (ties: the lowest indices).
+//                  then every warp counts the entries above it and the ties in its contiguous
+//                  index range (32 consecutive keys per step), the warps' counts place its kept
+//                  entries, and it writes them in ascending order (ties: the lowest indices).
 #include <mutex>
 
 #include "tv_common.cuh"
@@ -65,36 +65,6 @@ __global__ void score_kernel(int B, int64_t c4_cap, int d_idx, const uint16_t* _
   score[t] = s;
 }
 
-// Block-wide exclusive prefix sum of one int per thread (thread order); writes the block total to
-// *total.  `warp_tot` holds 33 ints of shared memory.
-__device__ __forceinline__ int block_exclusive_sum(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-    int z = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, z, o);
-      if (lane >= o) z += y;
-    }
-    warp_tot[lane] = z - w;
-    if (lane == 31) warp_tot[32] = z;
-  }
-  __syncthreads();
-  const int r = warp_tot[warp] + x - v;
-  *total = warp_tot[32];
-  __syncthreads();
-  return r;
-}
-
 __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int n_sel,
                                                              const int32_t* __restrict__ L,
                                                              const float* __restrict__ score,
@@ -102,11 +72,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
                                                              int32_t* status) {
   extern __shared__ uint32_t keys_smem[];
   __shared__ unsigned hist[256];
-  __shared__ int warp_tot[33];
+  __shared__ int warp_gt[32], warp_eq[32];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_krem;
   const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
   const int Lb = L[b];
   const int64_t n4 = Lb >= 0 ? Lb / 4 : -1;
   int32_t* out = sel + (int64_t)b * n_sel;
@@ -128,8 +99,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
     s_krem = n_sel;
   }
   __syncthreads();
-  // radix select of the n_sel-th largest key, most significant digit first.  Scores of one request
-  // share few exponents, so lanes of a warp that hit the same bin are merged before the atomic.
+  // radix select of the n_sel-th largest key, most significant digit first (shared-memory atomics
+  // measured faster here than merging equal bins within a warp first)
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
     __syncthreads();
@@ -141,50 +112,79 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
         const uint32_t key = key_at(j);
         if ((key & mask) == prefix) bin = (int)((key >> shift) & 255u);
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+      if (bin >= 0) atomicAdd(&hist[bin], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
+      // lane l holds bins 255-8l .. 248-8l (descending); an inclusive scan over lanes gives the
+      // count of keys in the digits above each lane's group
       const int krem = s_krem;
-      int above = 0;
-      int digit = 0;
-      for (int d = 255; d >= 0; --d) {
-        const int c = (int)hist[d];
-        if (above + c >= krem) {
-          digit = d;
-          break;
-        }
-        above += c;
+      int c[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c[q] = (int)hist[255 - 8 * lane - q];
+        sum += c[q];
       }
-      s_krem = krem - above;
-      s_prefix = prefix | ((uint32_t)digit << shift);
-      s_mask = mask | (255u << shift);
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - sum;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < krem && incl >= krem);
+      if (lane == __ffs(hit) - 1) {
+        int above = excl, digit = 0;
+        for (int q = 0; q < 8; ++q) {
+          if (above + c[q] >= krem) {
+            digit = 255 - 8 * lane - q;
+            break;
+          }
+          above += c[q];
+        }
+        s_krem = krem - above;
+        s_prefix = prefix | ((uint32_t)digit << shift);
+        s_mask = mask | (255u << shift);
+      }
     }
     __syncthreads();
   }
   const uint32_t T = s_prefix;   // key of the n_sel-th best entry
   const int need_eq = s_krem;    // entries with key == T to keep: the lowest-indexed ones
-  // thread t owns the contiguous index range [t * per, (t + 1) * per): count, scan, then write its
-  // kept entries in ascending order at their final positions
-  const int64_t per = (n4 + blockDim.x - 1) / blockDim.x;
-  const int64_t lo = threadIdx.x * per, hi = lo + per < n4 ? lo + per : n4;
+  // warp w owns the contiguous index range [w * R, (w + 1) * R), read 32 consecutive keys at a
+  // time: count, one scan over the warps, then write the kept entries in ascending order
+  const int n_warps = blockDim.x >> 5;
+  const int64_t R = (n4 + n_warps - 1) / n_warps;
+  const int64_t lo = warp * R, hi = lo + R < n4 ? lo + R : n4;
   int gt = 0, eq = 0;
-  for (int64_t j = lo; j < hi; ++j) {
-    const uint32_t key = key_at(j);
-    gt += key > T;
-    eq += key == T;
+  for (int64_t j0 = lo; j0 < hi; j0 += 32) {
+    const int64_t j = j0 + lane;
+    const uint32_t key = j < hi ? key_at(j) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, j < hi && key > T));
+    eq += __popc(__ballot_sync(0xffffffffu, j < hi && key == T));
   }
-  int gt_total, eq_total;
-  const int gt_before = block_exclusive_sum(gt, warp_tot, &gt_total);
-  const int eq_before = block_exclusive_sum(eq, warp_tot, &eq_total);
+  if (lane == 0) {
+    warp_gt[warp] = gt;
+    warp_eq[warp] = eq;
+  }
+  __syncthreads();
+  int gt_before = 0, eq_before = 0;
+  for (int w = 0; w < warp; ++w) {
+    gt_before += warp_gt[w];
+    eq_before += warp_eq[w];
+  }
   int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
-  int eq_rank = eq_before;
-  for (int64_t j = lo; j < hi; ++j) {
-    const uint32_t key = key_at(j);
-    bool take = key > T;
-    if (key == T) take = eq_rank++ < need_eq;
-    if (take) out[pos++] = (int32_t)j;
+  int eq_seen = eq_before;
+  for (int64_t j0 = lo; j0 < hi; j0 += 32) {
+    const int64_t j = j0 + lane;
+    const uint32_t key = j < hi ? key_at(j) : 0u;
+    const bool is_gt = j < hi && key > T, is_eq = j < hi && key == T;
+    const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
+    const bool take = is_gt || (is_eq && eq_seen + __popc(eqm & lt_mask) < need_eq);
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) out[pos + __popc(tm & lt_mask)] = (int32_t)j;
+    pos += __popc(tm);
+    eq_seen += __popc(eqm);
   }
 }
 
