@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the budget sweep instead of the bench line: D x batch x {chain, tree} x "
                          "child-match probability at prefix 4096, one JSON line per cell")
+    ap.add_argument("--draft", action="store_true",
+                    help="draft-side tree attention instead of the bench line: per draft step of "
+                         "a width-2 beam tree (B=64, serving cache geometry), one JSON line")
     ap.add_argument("--cells", type=str, default=None,
                     help="with --sweep: comma-separated cell indices (default: all 64)")
     return ap.parse_args()
@@ -637,6 +640,44 @@ def run_sweep(args):
                       "warmup": args.warmup, "best_committed_tokens_per_s": best}), flush=True)
 
 
+def run_draft(args):
+    """Draft decode at draft-side shapes: for draft steps s = 1..3 the tree built so far
+    (D_s = 1 + 2s nodes) goes through plan, scratch pad and attention; L2 flushed before each
+    timed iteration; CUDA events around the three calls."""
+    from tree_speculative_verify_gb300 import _lib, build as tvbuild, engine, workloads
+    tvbuild.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    base = workloads.draft_beam(B=args.batch or 64, steps=3)
+    for s in range(1, 4):
+        wl = workloads.draft_level(base, s)
+        shape = engine.shape_for(wl)
+        st = engine.alloc_state(wl)
+        rb = engine.alloc_round(wl, shape)
+        engine.prefill(shape, st, rb, stream)
+        for _ in range(args.warmup):
+            engine.draft_decode(shape, st, rb, None, stream)
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            engine.draft_decode(shape, st, rb, None, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        if int(rb.status.item()) != 0:
+            raise SystemExit(f"draft step {s}: device status {int(rb.status.item())}")
+        ms = statistics.median(ts)
+        print(json.dumps({"draft_step": s, "B": wl.B, "D": wl.D, "ms": ms,
+                          "draft_tree_tokens_per_s": wl.B * wl.D / (ms * 1e-3),
+                          "attention_kernel": "tcgen05" if _lib.tv_attn_kernel_for(shape) ==
+                          _lib.TV_ATTN_TCGEN05 else "simt"}), flush=True)
+        del st, rb
+        torch.cuda.empty_cache()
+
+
 def launches_per_step(shape, kernel):
     # plan, branch compress, accept, refresh + attention: SIMT (partials, merge; + the indexer's
     # two kernels on the sparse path) or tensor cores
@@ -660,6 +701,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.draft:
+        run_draft(args)
         return
     world, rank, local = dist_setup(args.gpus)
     try:

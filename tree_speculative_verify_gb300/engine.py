@@ -178,6 +178,17 @@ def verify_round(shape, st, rb, scale=None, stream=None, commit=True, select=Fal
         refresh(shape, st, rb, stream)
 
 
+def draft_decode(shape, st, rb, scale=None, stream=None):
+    """Draft-side tree attention ("Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for
+    Efficient Inference" §4.1, draft decode): every candidate of the draft tree built so far
+    attends to the prefix and its own ancestors, with the scratch pad isolating blocks closed
+    inside the tree -- the verify round's plan, scratch-pad and attention calls on the draft
+    step's tree, without acceptance or commit (nothing is accepted until the target verifies)."""
+    plan(shape, st, rb, stream)
+    branch_compress(shape, st, rb, stream)
+    attention(shape, st, rb, scale, stream)
+
+
 class RoundGraph:
     """One verify round captured as a CUDA graph on fixed buffers.
 

@@ -108,6 +108,31 @@ def build_tree(rng, k, steps, D):
     return parents
 
 
+def beam_tree(rng, k, steps):
+    """Parent array of a draft-side beam tree: the root's k children, then at every further level
+    the k best of the k x k children of the previous level's nodes (children get sorted U(0,1)
+    confidences, a node scores the product along its path; ties to the node created first).
+    1 + k * steps nodes, numbered level by level."""
+    parents, score = [-1], [1.0]
+    frontier = [0]
+    for lev in range(1, steps + 1):
+        cand = []
+        for u in frontier:
+            for c in np.sort(rng.random(k))[::-1]:
+                cand.append((u, score[u] * float(c)))
+        if lev == 1:
+            keep = cand
+        else:
+            order = sorted(range(len(cand)), key=lambda i: (-cand[i][1], i))[:k]
+            keep = [cand[i] for i in sorted(order)]
+        frontier = []
+        for u, sc in keep:
+            parents.append(u)
+            score.append(sc)
+            frontier.append(len(parents) - 1)
+    return np.asarray(parents, dtype=np.int32)
+
+
 def draw_tokens(rng, parents, p_match, forced=None):
     """Draft and target tokens of one tree (see module docstring).
 
@@ -151,7 +176,7 @@ def _caps(L_max, D):
 
 
 def make_workload(name, *, B, D, H, d, W, tail_mode, ms, dtype, L, k, steps, p_match, seed,
-                  kv_scale, n_sel=0, forced=None, fixed_parents=None):
+                  kv_scale, n_sel=0, forced=None, fixed_parents=None, beam=False):
     """Draw one workload.  ``L`` is an int (same for all requests) or a (lo, hi) uniform range."""
     rng = np.random.Generator(np.random.PCG64(seed))
     if isinstance(L, tuple):
@@ -162,8 +187,12 @@ def make_workload(name, *, B, D, H, d, W, tail_mode, ms, dtype, L, k, steps, p_m
     draft = np.empty((B, D), dtype=np.int32)
     target = np.empty((B, D), dtype=np.int32)
     for b in range(B):
-        par = np.asarray(fixed_parents, dtype=np.int32) if fixed_parents is not None \
-            else build_tree(rng, k, steps, D)
+        if fixed_parents is not None:
+            par = np.asarray(fixed_parents, dtype=np.int32)
+        elif beam:
+            par = beam_tree(rng, k, steps)
+        else:
+            par = build_tree(rng, k, steps, D)
         parents[b] = par
         draft[b], target[b] = draw_tokens(rng, par, p_match, forced)
     raw_cap, cap4, cap128 = _caps(int(Ls.max()), D)
@@ -252,3 +281,42 @@ def sweep_cell(idx, D, B, kind, p, L=4096):
     return make_workload(f"sweep_{kind}_D{D}_B{B}_p{p}", B=B, D=D, H=64, d=512, W=128,
                          tail_mode="window", ms=(4, 128), dtype="bf16", L=L, k=k, steps=steps,
                          p_match=p, seed=1000 + idx, kv_scale=0.5)
+
+
+def tree_depths(parents):
+    """Depth of every node of one parent array (root 0)."""
+    dep = np.zeros(len(parents), dtype=np.int64)
+    for v in range(1, len(parents)):
+        dep[v] = dep[int(parents[v])] + 1
+    return dep
+
+
+def draft_beam(seed=0, B=64, steps=3, L=(1024, 8192)):
+    """Draft-decode workload: the serving batch's cache geometry (C4 + C128 + 128 window, 64x1
+    heads, d = 512, bf16) with a width-2 beam tree of ``steps`` draft levels per request
+    (D = 1 + 2 * steps); ``draft_level`` cuts it to the tree the draft model attends over at each
+    step."""
+    return make_workload(f"draft_beam_B{B}_s{steps}", B=B, D=1 + 2 * steps, H=64, d=512, W=128,
+                         tail_mode="window", ms=(4, 128), dtype="bf16", L=L, k=2, steps=steps,
+                         p_match=0.55, seed=seed, kv_scale=0.5, beam=True)
+
+
+def draft_level(wl, s):
+    """The draft-decode view of a workload at draft step ``s``: every request's tree cut to its
+    nodes of depth <= s.  Nodes are numbered level by level, so these are the first D_s nodes; the
+    cut needs every request to have the same D_s (true of beam trees).  Queries, tree K/V and
+    tokens are sliced; the caches are shared."""
+    deps = [tree_depths(wl.parents[b]) for b in range(wl.B)]
+    counts = {int((d <= s).sum()) for d in deps}
+    if len(counts) != 1:
+        raise ValueError(f"requests have different node counts at depth <= {s}: {sorted(counts)}")
+    Ds = counts.pop()
+    cut = lambda a: np.ascontiguousarray(a[:, :Ds])
+    tcut = lambda t: t[:, :Ds].contiguous()
+    return Workload(name=f"{wl.name}_draft{s}", B=wl.B, D=Ds, H=wl.H, d=wl.d, W=wl.W,
+                    tail_mode=wl.tail_mode, ms=wl.ms, dtype=wl.dtype, L=wl.L, raw_cap=wl.raw_cap,
+                    cap4=wl.cap4, cap128=wl.cap128, parents=cut(wl.parents), draft=cut(wl.draft),
+                    target=cut(wl.target), Q=tcut(wl.Q), rawK=wl.rawK, rawV=wl.rawV,
+                    treeK=tcut(wl.treeK), treeV=tcut(wl.treeV), g=wl.g, sel=wl.sel,
+                    q_idx=wl.q_idx, k_idx=wl.k_idx, p_match=wl.p_match,
+                    meta=dict(wl.meta, draft_step=s))
