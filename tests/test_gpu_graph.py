@@ -53,3 +53,32 @@ def test_round_graph_replays_match_eager(case, kernel):
         got = _outputs(st, rb)
         for k, v in want.items():
             assert torch.equal(got[k], v), f"{k} differs after a graph replay"
+
+
+def test_sparse_round_graph_with_device_indexer_matches_eager():
+    # the long-context round: device indexer -> selection gather -> attention, captured once
+    wl = workloads.long_context(B=2, L=(9000, 12000), n_sel=512)
+    shape = engine.shape_for(wl)
+    st = engine.alloc_state(wl)
+    rb = engine.alloc_round(wl, shape)
+    engine.prefill(shape, st, rb)
+    torch.cuda.synchronize()
+    st_eager = st.clone()
+    rb_eager = engine.alloc_round(wl, shape)
+    L0 = st.L.clone()
+    engine.verify_round(shape, st_eager, rb_eager, select=True)
+    torch.cuda.synchronize()
+    assert int(rb_eager.status.item()) == 0
+    want = {k: v.clone() for k, v in _outputs(st_eager, rb_eager).items()}
+    want["sel"] = rb_eager.sel.clone()
+    graph = engine.RoundGraph(shape, st, rb, select=True,
+                              prologue=lambda: st.L.copy_(L0, non_blocking=True))
+    for _ in range(2):
+        rb.sel.fill_(-3)
+        rb.O.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(rb.status.item()) == 0
+        got = dict(_outputs(st, rb), sel=rb.sel)
+        for k, v in want.items():
+            assert torch.equal(got[k], v), f"{k} differs after a graph replay"

@@ -38,12 +38,15 @@ def _noalloc(shape, st, rb, O, lse):
         rb.scrV128, 1.0 / math.sqrt(shape.d), O, lse, rb.status)
 
 
-@pytest.mark.parametrize("case", ["small_split_kv", "tiny_fp32"])
+@pytest.mark.parametrize("case", ["small_split_kv", "tiny_fp32", "selection_list"])
 def test_noalloc_matches_workspace_entry_point_twice(case):
     if case == "small_split_kv":
         # 4 requests: the attention splits every request's KV over many CTAs, so the partials
         # fill most of the built-in scratch
         wl = workloads.small()
+    elif case == "selection_list":
+        # the tensor-core path gathers the selected C4 rows into the scratch first
+        wl = workloads.long_context(B=2, L=(9000, 12000), n_sel=512)
     else:
         wl = workloads.tiny(L=255)
     shape, st, rb = _prepared(wl)
