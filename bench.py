@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the budget sweep instead of the bench line: D x batch x {chain, tree} x "
                          "child-match probability at prefix 4096, one JSON line per cell")
+    ap.add_argument("--page-tokens", type=int, default=0,
+                    help="keep the persistent cache in page pools of this many tokens per page "
+                         "(a multiple of 512; pages scattered over the pool); 0 = contiguous")
     ap.add_argument("--draft", action="store_true",
                     help="draft-side tree attention instead of the bench line: per draft step of "
                          "a width-2 beam tree (B=64, serving cache geometry), one JSON line")
@@ -392,8 +395,15 @@ def run_ours(args, world, rank, local):
     shape = engine.shape_for(wl, kernel)
     stream = torch.cuda.current_stream()
     sets = []
-    for _ in range(n_sets):
-        st = engine.alloc_state(wl)
+    for i in range(n_sets):
+        if args.page_tokens:
+            # every copy gets the same (seeded) page table, so the first copy's shape -- which
+            # holds the address of its table -- serves all of them
+            shape_i, st = engine.alloc_paged(wl, args.page_tokens, kernel, seed=0)
+            if i == 0:
+                shape = shape_i
+        else:
+            st = engine.alloc_state(wl)
         rb = engine.alloc_round(wl, shape)
         engine.prefill(shape, st, rb, stream)
         sets.append((st, rb, st.L.clone()))
@@ -551,7 +561,9 @@ def run_ours(args, world, rank, local):
                    "l2": f"inputs larger than L2: {n_sets} rotating state copies, "
                          f"{kv_bytes / 1e6:.0f} MB KV per step each",
                    "parallelism": f"replicas x{world} (requests sharded, no collective)",
-                   "cuda_graph": graphs is not None},
+                   "cuda_graph": graphs is not None,
+                   "kv_layout": (f"page pools, {args.page_tokens} tokens per page, pages scattered"
+                                 if args.page_tokens else "contiguous per request")},
         "roofline": {"bound": "tensor", "achieved": tflops,
                      "peak": pk["tc"], "unit": "TFLOP/s", "frac": tflops / pk["tc"],
                      "traffic": traffic,

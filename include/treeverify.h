@@ -102,6 +102,19 @@ typedef struct tv_shape {
   int64_t raw_cap;     /* rows per request of rawK / rawV */
   int64_t c4_cap;      /* rows per request of c4K / c4V (ignored without C4) */
   int64_t c128_cap;    /* rows per request of c128K / c128V (ignored without C128) */
+  /* Page-based persistent cache ([TSD-V4] §4.2: one logical layer over three physical layers
+   * with shared page pointers).  page_tokens == 0: rawK/rawV, c4K/c4V, c128K/c128V are
+   * contiguous [B][cap][d] arrays.  page_tokens == P > 0 (a multiple of 512): they are page pools
+   * of n_pool_pages pages -- rawK [n_pool_pages][P][d], c4K [n_pool_pages][P/4][d],
+   * c128K [n_pool_pages][P/128][d] (V alike) -- and logical page g of request b (tokens
+   * g*P .. g*P+P-1, with their C4 and C128 entries) lives in page page_table[b][g] of all three;
+   * raw_cap, c4_cap and c128_cap must then be max_pages * P, * P/4 and * P/128.  A page id outside
+   * 0 .. n_pool_pages-1 is reported as TV_ERR_ARG on the device (and page 0 is read instead). */
+  int32_t page_tokens;
+  int32_t max_pages;           /* logical pages per request (columns of page_table) */
+  int32_t n_pool_pages;        /* pages in each pool */
+  int32_t reserved;            /* must be 0 */
+  const int32_t* page_table;   /* device [B][max_pages] int32 (page_tokens > 0 only) */
 } tv_shape;
 
 /* Library version string (static storage). */

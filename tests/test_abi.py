@@ -55,7 +55,7 @@ def test_version_and_status_strings(lib):
 
 
 def test_struct_layout_matches_c():
-    assert ctypes.sizeof(_lib.tv_shape) == 10 * 4 + 3 * 8
+    assert ctypes.sizeof(_lib.tv_shape) == 10 * 4 + 3 * 8 + 4 * 4 + 8
 
 
 def _shape(**kw):
@@ -108,3 +108,15 @@ def test_indexer_validation(lib):
     rc = lib.tv_indexer_topk(ctypes.byref(s), 64, None, None, None, None, None, 0, None, None)
     assert rc == -1                                           # null inputs
     assert lib.tv_indexer_workspace_size(ctypes.byref(s)) == 2304         # 2 x 260 x 4, to 256
+
+
+def test_paging_validation(lib):
+    # page size not a multiple of 512; capacities inconsistent with the pages; no page table
+    s = _shape(page_tokens=300, max_pages=4, n_pool_pages=8)
+    assert lib.tv_accept_walk(ctypes.byref(s), *([None] * 8)) == -2
+    s = _shape(page_tokens=512, max_pages=2, n_pool_pages=8, raw_cap=1024, c4_cap=256, c128_cap=9)
+    assert lib.tv_accept_walk(ctypes.byref(s), *([None] * 8)) == -2
+    s = _shape(page_tokens=512, max_pages=2, n_pool_pages=8, raw_cap=1024, c4_cap=256, c128_cap=8)
+    assert lib.tv_accept_walk(ctypes.byref(s), *([None] * 8)) == -1      # page_table is null
+    s.reserved = 1
+    assert lib.tv_workspace_size(ctypes.byref(s)) == 0

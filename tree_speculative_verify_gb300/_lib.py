@@ -41,7 +41,9 @@ class tv_shape(ctypes.Structure):
         ("d", ctypes.c_int32), ("W", ctypes.c_int32), ("tail_mode", ctypes.c_int32),
         ("comp_mask", ctypes.c_int32), ("dtype", ctypes.c_int32), ("n_sel", ctypes.c_int32),
         ("attn_kernel", ctypes.c_int32), ("raw_cap", ctypes.c_int64), ("c4_cap", ctypes.c_int64),
-        ("c128_cap", ctypes.c_int64),
+        ("c128_cap", ctypes.c_int64), ("page_tokens", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32), ("n_pool_pages", ctypes.c_int32),
+        ("reserved", ctypes.c_int32), ("page_table", ctypes.c_void_p),
     ]
 
 
@@ -100,9 +102,13 @@ def version():
 
 
 def make_shape(*, B, D, H, d, W=0, tail_mode=TV_TAIL_WINDOW, comp_mask=TV_COMP_C4 | TV_COMP_C128,
-               dtype=TV_BF16, n_sel=0, attn_kernel=TV_ATTN_AUTO, raw_cap=0, c4_cap=0, c128_cap=0):
+               dtype=TV_BF16, n_sel=0, attn_kernel=TV_ATTN_AUTO, raw_cap=0, c4_cap=0, c128_cap=0,
+               page_tokens=0, max_pages=0, n_pool_pages=0, page_table=None):
+    """``page_table``: a CUDA int32 tensor [B][max_pages] (paged pools only); the shape keeps its
+    device address, so the tensor must outlive the shape's use."""
+    pt = None if page_table is None else _p(page_table).value
     return tv_shape(B, D, H, d, W, tail_mode, comp_mask, dtype, n_sel, attn_kernel, raw_cap,
-                    c4_cap, c128_cap)
+                    c4_cap, c128_cap, page_tokens, max_pages, n_pool_pages, 0, pt)
 
 
 def _p(t):

@@ -77,6 +77,23 @@ static int check_shape(const tv_shape* s, const char* fn) {
     return tv_set_error(TV_ERR_SHAPE, "%s: capacities must be in 0..2^30", fn);
   if ((int64_t)s->B * s->D * s->H > ((int64_t)1 << 31) / 1024)
     return tv_set_error(TV_ERR_SHAPE, "%s: B*D*H too large", fn);
+  if (s->reserved != 0) return tv_set_error(TV_ERR_ARG, "%s: reserved field must be 0", fn);
+  if (s->page_tokens != 0) {
+    const int64_t P = s->page_tokens, G = s->max_pages;
+    if (P < 0 || P % 512 != 0 || P > (1 << 20))
+      return tv_set_error(TV_ERR_SHAPE, "%s: page_tokens = %d is not a multiple of 512", fn,
+                          s->page_tokens);
+    if (G < 1 || s->n_pool_pages < 1 || (int64_t)s->n_pool_pages * P > ((int64_t)1 << 31))
+      return tv_set_error(TV_ERR_SHAPE, "%s: max_pages = %d / n_pool_pages = %d out of range", fn,
+                          s->max_pages, s->n_pool_pages);
+    if (s->raw_cap != G * P || s->c4_cap != G * P / 4 || s->c128_cap != G * P / 128)
+      return tv_set_error(TV_ERR_SHAPE,
+                          "%s: with pages, raw_cap / c4_cap / c128_cap must be max_pages * P, "
+                          "* P/4, * P/128",
+                          fn);
+    if (s->B > 0 && s->page_table == nullptr)
+      return tv_set_error(TV_ERR_ARG, "%s: page_table is null", fn);
+  }
   return TV_OK;
 }
 
@@ -267,6 +284,7 @@ static tv::AttnParams<T> make_params(const tv_shape* s, const void* Q, const voi
   p.raw_cap = s->raw_cap;
   p.c4_cap = s->c4_cap;
   p.c128_cap = s->c128_cap;
+  p.pg = tv::paging_of(s);
   p.Q = (const T*)Q;
   p.c4K = (const T*)c4K;
   p.c4V = (const T*)c4V;

@@ -19,6 +19,7 @@ template <typename T>
 struct AttnParams {
   int B, D, H, d, W, tail_mode, comp_mask, n_sel;
   int64_t raw_cap, c4_cap, c128_cap;
+  Paging pg;
   const T* Q;
   const T* c4K;
   const T* c4V;
@@ -110,18 +111,18 @@ __device__ __forceinline__ EntryRef resolve_entry(const AttnParams<T>& p, const 
         return r;
       }
     }
-    const int64_t off = ((int64_t)b * p.c4_cap + j) * d;
+    const int64_t off = layer_row(p.pg, b, j, p.c4_cap, 4, p.status) * d;
     r.k = p.c4K + off;
     r.v = p.c4V + off;
     r.kind = kEntryShared;
   } else if (e < lay.baseraw) {
-    const int64_t off = ((int64_t)b * p.c128_cap + (e - lay.base128)) * d;
+    const int64_t off = layer_row(p.pg, b, e - lay.base128, p.c128_cap, 128, p.status) * d;
     r.k = p.c128K + off;
     r.v = p.c128V + off;
     r.kind = kEntryShared;
   } else if (e < lay.basetree) {
     const int pos = lay.t0 + (e - lay.baseraw);
-    const int64_t off = ((int64_t)b * p.raw_cap + pos) * d;
+    const int64_t off = layer_row(p.pg, b, pos, p.raw_cap, 1, p.status) * d;
     r.k = p.rawK + off;
     r.v = p.rawV + off;
     r.kind = kEntryRaw;

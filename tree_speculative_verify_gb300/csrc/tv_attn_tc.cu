@@ -91,6 +91,9 @@ struct Params {
   float* part;          // split-KV partials (n_chunks > 1)
   const int32_t* order; // requests by decreasing tile count (longest first)
   int32_t* status;
+  Paging pg;       // paged pools: C4 tiles are read through the page table; the C128 entries and
+                   // the raw tail are first gathered into the workspace (contiguous per request)
+  int tail_rows;   // rows per request of the gathered raw tail (paged pools only)
 };
 
 struct Layout {
@@ -166,7 +169,8 @@ __global__ void order_kernel(Params p, int32_t* order) {
 // into row i of a dense per-request buffer, so the attention kernel reads the selection as
 // contiguous tiles.  One warp per selected entry; an index outside 0 .. L/4 - 1 (or past the C4
 // capacity) records TV_ERR_SELECTION and leaves a zero row.
-__global__ void gather_sel_kernel(int B, int n_sel, int64_t c4_cap, const int32_t* __restrict__ L,
+__global__ void gather_sel_kernel(Paging pg, int B, int n_sel, int64_t c4_cap,
+                                  const int32_t* __restrict__ L,
                                   const int32_t* __restrict__ sel, const uint4* __restrict__ c4K,
                                   const uint4* __restrict__ c4V, uint4* __restrict__ gK,
                                   uint4* __restrict__ gV, int32_t* status) {
@@ -179,12 +183,63 @@ __global__ void gather_sel_kernel(int B, int n_sel, int64_t c4_cap, const int32_
   const bool ok = Lb >= 0 && j >= 0 && j < Lb / 4 && j < c4_cap;
   if (!ok && lane == 0) record_error(status, TV_ERR_SELECTION);
   constexpr int kRowU4 = 512 * 2 / 16;   // 64 x 16 B per bf16 row of 512
-  const int64_t src = ((int64_t)b * c4_cap + (ok ? j : 0)) * kRowU4;
+  const int64_t src = ok ? layer_row(pg, b, j, c4_cap, 4, status) * kRowU4 : 0;
   const int64_t dst = w * kRowU4;
   for (int i = lane; i < kRowU4; i += 32) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     gK[dst + i] = ok ? c4K[src + i] : z;
     gV[dst + i] = ok ? c4V[src + i] : z;
+  }
+}
+
+// Paged pools: copies each request's C128 entries 0 .. c128_cap-1 and its raw tail (positions
+// t0 .. t0 + tail_rows - 1) from the pools into contiguous workspace rows; rows past L/128 or past
+// L are zero (the attention loads whole 64-row boxes and masks the extra entries, so they must be
+// finite).  One warp per row; grid.y = request.
+__global__ void gather_paged_kernel(Paging pg, int comp_mask, int W, int tail_mode,
+                                    int64_t raw_cap, int64_t c128_cap, int tail_rows,
+                                    const int32_t* __restrict__ L, const uint4* __restrict__ c128K,
+                                    const uint4* __restrict__ c128V, const uint4* __restrict__ rawK,
+                                    const uint4* __restrict__ rawV, uint4* gK128, uint4* gV128,
+                                    uint4* gKraw, uint4* gVraw, int32_t* status) {
+  constexpr int kRowU4 = 512 * 2 / 16;
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int Lb = L[b];
+  const bool c128 = comp_mask & TV_COMP_C128;
+  const int64_t n128 = c128 ? c128_cap : 0;
+  const int tail = tail_mode == TV_TAIL_WINDOW ? W : m_min_of(comp_mask) - 1;
+  const int t0 = Lb - tail > 0 ? Lb - tail : 0;
+  const bool ok = Lb >= 0 && Lb <= raw_cap;
+  const int64_t rows = n128 + tail_rows;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; w < rows;
+       w += (int64_t)gridDim.x * (blockDim.x / 32)) {
+    const uint4* sK = nullptr;
+    const uint4* sV = nullptr;
+    uint4 *dK, *dV;
+    if (w < n128) {
+      if (ok && w < Lb / 128) {
+        const int64_t r = layer_row(pg, b, w, c128_cap, 128, status);
+        sK = c128K + r * kRowU4;
+        sV = c128V + r * kRowU4;
+      }
+      dK = gK128 + ((int64_t)b * c128_cap + w) * kRowU4;
+      dV = gV128 + ((int64_t)b * c128_cap + w) * kRowU4;
+    } else {
+      const int64_t pos = t0 + (w - n128);
+      if (ok && pos < Lb) {
+        const int64_t r = layer_row(pg, b, pos, raw_cap, 1, status);
+        sK = rawK + r * kRowU4;
+        sV = rawV + r * kRowU4;
+      }
+      dK = gKraw + ((int64_t)b * tail_rows + (w - n128)) * kRowU4;
+      dV = gVraw + ((int64_t)b * tail_rows + (w - n128)) * kRowU4;
+    }
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = lane; i < kRowU4; i += 32) {
+      dK[i] = sK ? sK[i] : z;
+      dV[i] = sV ? sV[i] : z;
+    }
   }
 }
 
@@ -211,12 +266,24 @@ __device__ __forceinline__ void fail(Smem& sm, int32_t* status) {
   if (atomicExch(&sm.abort, 1) == 0) record_error(status, TV_ERR_TIMEOUT);
 }
 
-__device__ __forceinline__ int64_t base_row(const Params& p, int kind, int b) {
-  return kind == kC4 ? (int64_t)b * p.c4_cap : kind == kC128 ? (int64_t)b * p.c128_cap
-                                                             : (int64_t)b * p.raw_cap;
+// Row (in its tensor map) of entry `idx` of a C4 / C128 / raw tile of request b.  Contiguous
+// caches: b * cap + idx.  Paged pools: C4 rows through the page table (a 64-row box never crosses
+// a C4 page: a page holds a multiple of 128 entries and tiles start at multiples of 128); C128
+// entries and raw positions from the gathered copies in the workspace.
+template <bool kPaged>
+__device__ __forceinline__ int64_t tile_row(const Params& p, int kind, int b, int64_t idx,
+                                            int t0) {
+  if (kind == kC4) {
+    if (kPaged && p.n_sel == 0) return layer_row(p.pg, b, idx, p.c4_cap, 4, p.status);
+    return (int64_t)b * p.c4_cap + idx;
+  }
+  if (kind == kC128) return (int64_t)b * p.c128_cap + idx;
+  if (kPaged) return (int64_t)b * p.tail_rows + (idx - t0);
+  return (int64_t)b * p.raw_cap + idx;
 }
 
 // ---- producer (warp 0 of both CTAs) --------------------------------------------------------
+template <bool kPaged>
 __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uint32_t rank,
                          const Layout& y, int tb, int te) {
   const int lane = threadIdx.x & 31;
@@ -257,7 +324,22 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
   };
   // S operand: this CTA holds entries [rank * nqk/2, (rank+1) * nqk/2) of the tile; one slot
   // holds four 64-dim slices of those (up to 64) entries, 8 KB each.
-  auto load_k = [&](const Tile& x) -> bool {
+  // rows of a tile's boxes (this CTA's K half, the two V halves), computed one tile ahead so that
+  // with paged pools the page-table reads are in flight while the producer waits for slots
+  struct Rows {
+    int k, v0, v1;
+  };
+  auto rows_of = [&](int t) -> Rows {
+    Rows r{0, 0, 0};
+    if (t < tb || t >= te) return r;
+    const Tile x = tile_of(y, t);
+    if (x.kind == kExtra) return r;
+    r.k = (int)tile_row<kPaged>(p, x.kind, b, x.row0 + (int)rank * (x.nqk / 2), y.t0);
+    r.v0 = (int)tile_row<kPaged>(p, x.kind, b, x.row0, y.t0);
+    r.v1 = kPaged ? (int)tile_row<kPaged>(p, x.kind, b, x.row0 + 64, y.t0) : r.v0 + 64;
+    return r;
+  };
+  auto load_k = [&](const Tile& x, const Rows& rw) -> bool {
     const int nh = x.nqk / 2;
     for (int j = 0; j < 512 / (64 * kKSlices); ++j) {
       if (!acquire()) return false;
@@ -280,7 +362,7 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
           }
         } else {
           const CUtensorMap* m = x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
-          const int r = (int)(base_row(p, x.kind, b) + x.row0 + (int)rank * nh);
+          const int r = rw.k;
           expect(kSlotBytes);
           for (int ks = 0; ks < kKSlices; ++ks)
             tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * j + ks), r, bar);
@@ -293,7 +375,7 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
   // PV operand: every entry of the tile, this CTA's 128 of the pair's 256 value columns; one slot
   // holds the tile's entries as two 64-column blocks of 128 rows (rows past the tile's entry
   // count rounded up to 64 are not loaded).
-  auto load_v = [&](const Tile& x) -> bool {
+  auto load_v = [&](const Tile& x, const Rows& rw) -> bool {
     const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
     const int col0 = 256 * half + 128 * (int)rank;
     {
@@ -313,11 +395,12 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
           }
         } else {
           const CUtensorMap* m = x.kind == kC4 ? &p.mC4V : x.kind == kC128 ? &p.mC128V : &p.mRawV;
-          const int r = (int)(base_row(p, x.kind, b) + x.row0);
           expect(nvh * 2 * 8192);
-          for (int h = 0; h < nvh; ++h)
+          for (int h = 0; h < nvh; ++h) {
+            const int r = h == 0 ? rw.v0 : rw.v1;
             for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb, r + 64 * h, bar);
+              tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb, r, bar);
+          }
         }
       }
       advance();
@@ -325,11 +408,15 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
     return true;
   };
   bool ok = true;
+  Rows prev = rows_of(tb - 1), cur = rows_of(tb);
   for (int t = tb; t < te && ok; ++t) {
-    ok = load_k(tile_of(y, t));
-    if (ok && t > tb) ok = load_v(tile_of(y, t - 1));
+    const Rows next = rows_of(t + 1);
+    ok = load_k(tile_of(y, t), cur);
+    if (ok && t > tb) ok = load_v(tile_of(y, t - 1), prev);
+    prev = cur;
+    cur = next;
   }
-  if (ok && te > tb) load_v(tile_of(y, te - 1));
+  if (ok && te > tb) load_v(tile_of(y, te - 1), prev);
   // drain: no copy issued by the pair may still be in flight when the CTA exits (the leader's
   // full barriers count both CTAs' shares; the closing cluster barrier covers the follower)
   if (rank == 0)
@@ -658,6 +745,10 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
   }
 }
 
+// kPaged: the persistent cache is in page pools (C4 tiles through the page table, C128 entries
+// and the raw tail from gathered copies); a separate instantiation keeps the contiguous path's
+// producer free of the page-table work.
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
@@ -719,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 
   if (tb < te) {
     if (warp == 0) {
-      producer(p, sm, b, rt, half, rank, y, tb, te);
+      producer<kPaged>(p, sm, b, rt, half, rank, y, tb, te);
     } else if (warp == 1) {
       if (lane == 0) {
         if (rank == 0) mma_issuer(p, sm, y, tb, te);
@@ -839,10 +930,25 @@ static size_t order_bytes(const tv_shape* s) { return ((size_t)s->B * 4 + 255) /
 static size_t gather_bytes(const tv_shape* s) {
   return s->n_sel > 0 ? (size_t)s->B * s->n_sel * 512 * 2 : 0;   // one of K / V (multiple of 1 KB)
 }
+// Paged pools: rows per request of the gathered raw tail (a whole number of 128-row tiles).
+static int tail_rows_of(const tv_shape* s) {
+  const int tail = s->tail_mode == TV_TAIL_WINDOW ? s->W : tv::m_min_of(s->comp_mask) - 1;
+  return 128 * (((tail > 0 ? tail : 1) + 127) / 128);
+}
+static size_t paged_c128_bytes(const tv_shape* s) {   // one of K / V
+  return s->page_tokens > 0 && (s->comp_mask & TV_COMP_C128) ? (size_t)s->B * s->c128_cap * 1024
+                                                               : 0;
+}
+static size_t paged_raw_bytes(const tv_shape* s) {    // one of K / V
+  return s->page_tokens > 0 ? (size_t)s->B * tail_rows_of(s) * 1024 : 0;
+}
+static size_t pre_partial_bytes(const tv_shape* s) {
+  return order_bytes(s) + 2 * gather_bytes(s) + 2 * paged_c128_bytes(s) + 2 * paged_raw_bytes(s);
+}
 
 size_t tv_tc_workspace_size(const tv_shape* s) {
   const int n = tc_chunks(s);
-  size_t bytes = order_bytes(s) + 2 * gather_bytes(s);
+  size_t bytes = pre_partial_bytes(s);
   if (n > 1) bytes += (size_t)s->B * s->D * s->H * n * (s->d + 4) * sizeof(float);
   return bytes;
 }
@@ -863,24 +969,50 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
     c4K = ws + order_bytes(s);
     c4V = ws + order_bytes(s) + gather_bytes(s);
   }
+  const bool paged = s->page_tokens > 0;
   const void* c128K = c128 ? a.c128K : a.rawK;
   const void* c128V = c128 ? a.c128V : a.rawV;
+  const void* rawK = a.rawK;
+  const void* rawV = a.rawV;
+  char* g128 = ws + order_bytes(s) + 2 * gather_bytes(s);
+  char* graw = g128 + 2 * paged_c128_bytes(s);
+  if (paged) {
+    if (c128) {
+      c128K = g128;
+      c128V = g128 + paged_c128_bytes(s);
+    }
+    rawK = graw;
+    rawV = graw + paged_raw_bytes(s);
+  }
   const void* s4K = c4 ? a.scrK4 : a.treeK;
   const void* s4V = c4 ? a.scrV4 : a.treeV;
   const void* s128K = c128 ? a.scrK128 : a.treeK;
   const void* s128V = c128 ? a.scrV128 : a.treeV;
   auto rows_or_one = [](uint64_t r) { return r > 0 ? r : (uint64_t)1; };
-  const uint64_t c4rows =
-      rows_or_one(B * (uint64_t)(gathered ? s->n_sel : c4 ? s->c4_cap : s->raw_cap));
-  const uint64_t c128rows = rows_or_one(B * (uint64_t)(c128 ? s->c128_cap : s->raw_cap));
-  const uint64_t rawrows = rows_or_one(B * (uint64_t)s->raw_cap);
+  // rows of each map: contiguous caches B x cap; paged C4 pool pages x P/4; gathered copies B x n
+  const uint64_t rawrows = rows_or_one(paged ? B * (uint64_t)tail_rows_of(s)
+                                             : B * (uint64_t)s->raw_cap);
+  const uint64_t c4rows = rows_or_one(
+      gathered ? B * (uint64_t)s->n_sel
+               : !c4 ? rawrows
+                     : paged ? (uint64_t)s->n_pool_pages * (s->page_tokens / 4)
+                             : B * (uint64_t)s->c4_cap);
+  const uint64_t c128rows = rows_or_one(c128 ? B * (uint64_t)s->c128_cap : rawrows);
+  if (!c4) {
+    c4K = rawK;
+    c4V = rawV;
+  }
+  if (!c128) {
+    c128K = rawK;
+    c128V = rawV;
+  }
   const uint64_t trows = B * (uint64_t)s->D;
   bool ok = make_map(&p.mQ, a.Q, 3, DH, B, 128);
   ok = ok && make_map(&p.mC4K, c4K, 2, c4rows, 1, 64) && make_map(&p.mC4V, c4V, 2, c4rows, 1, 64);
   ok = ok && make_map(&p.mC128K, c128K, 2, c128rows, 1, 64) &&
        make_map(&p.mC128V, c128V, 2, c128rows, 1, 64);
-  ok = ok && make_map(&p.mRawK, a.rawK, 2, rawrows, 1, 64) &&
-       make_map(&p.mRawV, a.rawV, 2, rawrows, 1, 64);
+  ok = ok && make_map(&p.mRawK, rawK, 2, rawrows, 1, 64) &&
+       make_map(&p.mRawV, rawV, 2, rawrows, 1, 64);
   ok = ok && make_map(&p.mTreeK, a.treeK, 2, trows, 1, kDp) &&
        make_map(&p.mTreeV, a.treeV, 2, trows, 1, kDp);
   ok = ok && make_map(&p.mS4K, s4K, 2, trows, 1, kDp) && make_map(&p.mS4V, s4V, 2, trows, 1, kDp);
@@ -901,6 +1033,8 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.c4_cap = gathered ? s->n_sel : s->c4_cap;
   p.n_sel = gathered ? s->n_sel : 0;
   p.c128_cap = s->c128_cap;
+  p.pg = tv::paging_of(s);
+  p.tail_rows = tail_rows_of(s);
   p.L = a.L;
   p.raw_lo = a.raw_lo;
   p.anc = a.anc;
@@ -911,15 +1045,27 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.lse = a.lse;
   int32_t* order = reinterpret_cast<int32_t*>(workspace);
   p.order = order;
-  p.part = reinterpret_cast<float*>(ws + order_bytes(s) + 2 * gather_bytes(s));
+  p.part = reinterpret_cast<float*>(ws + pre_partial_bytes(s));
   p.status = a.status;
   if (gathered && s->B > 0) {
     const int64_t rows = (int64_t)s->B * s->n_sel;
     gather_sel_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        s->B, s->n_sel, s->c4_cap, a.L, a.sel, reinterpret_cast<const uint4*>(a.c4K),
+        tv::paging_of(s), s->B, s->n_sel, s->c4_cap, a.L, a.sel, reinterpret_cast<const uint4*>(a.c4K),
         reinterpret_cast<const uint4*>(a.c4V), reinterpret_cast<uint4*>(ws + order_bytes(s)),
         reinterpret_cast<uint4*>(ws + order_bytes(s) + gather_bytes(s)), a.status);
     if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 selection gather)")) return rc;
+  }
+  if (paged && s->B > 0) {
+    const int64_t rows = (c128 ? s->c128_cap : 0) + tail_rows_of(s);
+    const unsigned gx = (unsigned)((rows + 7) / 8 < 4096 ? (rows + 7) / 8 : 4096);
+    gather_paged_kernel<<<dim3(gx, s->B), 256, 0, stream>>>(
+        tv::paging_of(s), s->comp_mask, s->W, s->tail_mode, s->raw_cap, s->c128_cap,
+        tail_rows_of(s), a.L, reinterpret_cast<const uint4*>(a.c128K),
+        reinterpret_cast<const uint4*>(a.c128V), reinterpret_cast<const uint4*>(a.rawK),
+        reinterpret_cast<const uint4*>(a.rawV), reinterpret_cast<uint4*>(g128),
+        reinterpret_cast<uint4*>(g128 + paged_c128_bytes(s)), reinterpret_cast<uint4*>(graw),
+        reinterpret_cast<uint4*>(graw + paged_raw_bytes(s)), a.status);
+    if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 paged gather)")) return rc;
   }
   // one CTA ranks all requests (B <= 12288 fits its default shared memory)
   order_kernel<<<1, 1024, (size_t)s->B * sizeof(int), stream>>>(p, order);
@@ -934,7 +1080,9 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   {
     std::lock_guard<std::mutex> lock(attr_mu);
     if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess ||
+          cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem) != cudaSuccess)
         return tv_check_launch("tv_tree_verify_attn (tcgen05 shared-memory attribute)");
       attr_set[dev] = true;
@@ -953,7 +1101,9 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_kernel, p) != cudaSuccess)
+  const cudaError_t le = paged ? cudaLaunchKernelEx(&cfg, attn_kernel<true>, p)
+                               : cudaLaunchKernelEx(&cfg, attn_kernel<false>, p);
+  if (le != cudaSuccess)
     return tv_check_launch("tv_tree_verify_attn (tcgen05 pair launch)");
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05)")) return rc;
   if (p.n_chunks > 1)

@@ -43,6 +43,42 @@ __host__ __device__ __forceinline__ int m_min_of(int comp_mask) {
   return (comp_mask & TV_COMP_C4) ? 4 : 128;
 }
 
+// Persistent-row addressing, contiguous or paged (see tv_shape).  A layer whose rows each cover
+// `tokens_per_row` positions (raw 1, C4 4, C128 128) has page_tokens / tokens_per_row rows per page.
+struct Paging {
+  int32_t page_tokens;   // 0: contiguous [B][cap] rows
+  int32_t max_pages;
+  int32_t n_pool_pages;
+  const int32_t* table;  // [B][max_pages]
+};
+
+inline Paging paging_of(const tv_shape* s) {
+  Paging p;
+  p.page_tokens = s->page_tokens;
+  p.max_pages = s->max_pages;
+  p.n_pool_pages = s->n_pool_pages;
+  p.table = s->page_table;
+  return p;
+}
+
+// Row of row `idx` of request b in a layer with `cap` rows per request.  A page id outside the
+// pool records TV_ERR_ARG and addresses page 0 (so no access leaves the pool).  With pages, an
+// index past the request's capacity (the padding rows of a partial tile, never used unmasked) is
+// clamped to its last row, so the page-table read stays inside the request's row of the table.
+__device__ __forceinline__ int64_t layer_row(const Paging& pg, int b, int64_t idx, int64_t cap,
+                                             int tokens_per_row, int32_t* status) {
+  if (pg.page_tokens == 0) return (int64_t)b * cap + idx;
+  if (idx >= cap) idx = cap - 1;
+  if (idx < 0) idx = 0;
+  const int64_t rpp = pg.page_tokens / tokens_per_row;
+  int32_t page = pg.table[(int64_t)b * pg.max_pages + idx / rpp];
+  if (page < 0 || page >= pg.n_pool_pages) {
+    record_error(status, TV_ERR_ARG);
+    page = 0;
+  }
+  return (int64_t)page * rpp + idx % rpp;
+}
+
 }  // namespace tv
 
 // Host-side helpers shared by the entry points (defined in tv_api.cu).

@@ -207,7 +207,7 @@ __device__ void gated_block_sum(const T* const* rowK, const T* const* rowV, int 
 // ---- prefill: every complete block of the committed prefix ---------------------------------
 // grid.x: entry index (strided), grid.y: request.
 template <typename T>
-__global__ void __launch_bounds__(kCompressThreads, 2) prefill_kernel(int m, int d, int64_t raw_cap, int64_t cap_m,
+__global__ void __launch_bounds__(kCompressThreads, 2) prefill_kernel(Paging pg, int m, int d, int64_t raw_cap, int64_t cap_m,
                                const T* __restrict__ rawK, const T* __restrict__ rawV,
                                const int32_t* __restrict__ L, const float* __restrict__ g,
                                T* __restrict__ CK, T* __restrict__ CV, int32_t* status) {
@@ -224,12 +224,12 @@ __global__ void __launch_bounds__(kCompressThreads, 2) prefill_kernel(int m, int
   const int n = Lb / m;
   for (int j = blockIdx.x; j < n; j += gridDim.x) {
     for (int t = threadIdx.x; t < m; t += blockDim.x) {
-      const int64_t row = (int64_t)b * raw_cap + (int64_t)j * m + t;
+      const int64_t row = layer_row(pg, b, (int64_t)j * m + t, raw_cap, 1, status);
       rowK[t] = rawK + row * d;
       rowV[t] = rawV + row * d;
     }
     __syncthreads();
-    const int64_t out = ((int64_t)b * cap_m + j) * d;
+    const int64_t out = layer_row(pg, b, j, cap_m, m, status) * d;
     gated_block_sum<T>(rowK, rowV, m, d, g, CK + out, CV + out, w, red);
     __syncthreads();
   }
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) prefill_kernel(int m, int
 // with the block that v's token closes (positions pos_v - m + 1 .. pos_v of prefix + path(v)) or
 // with zeros.
 template <typename T>
-__global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(int D, int d, int comp_mask, int64_t raw_cap,
+__global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(Paging pg, int D, int d, int comp_mask, int64_t raw_cap,
                               const T* __restrict__ rawK, const T* __restrict__ rawV,
                               const int32_t* __restrict__ L, const T* __restrict__ treeK,
                               const T* __restrict__ treeV, const int32_t* __restrict__ parents,
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(int D, int 
   for (int t = threadIdx.x; t < m; t += blockDim.x) {
     const int p = pos + 1 - m + t;   // >= 0 because pos + 1 is a positive multiple of m
     if (p < Lb) {
-      const int64_t row = (int64_t)b * raw_cap + p;
+      const int64_t row = layer_row(pg, b, p, raw_cap, 1, status);
       rowK[t] = rawK + row * d;
       rowV[t] = rawV + row * d;
     } else {
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(int D, int 
 // One CTA per request.  Copies the accepted tokens' K/V into the raw rows L .. L+n-1 and the
 // scratch rows of accepted nodes that close a block into the persistent entries (all rows in
 // parallel: each 16-byte chunk of each row is one thread's job), then advances L.
-__global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_cap,
+__global__ void refresh_kernel(Paging pg, int D, int d, int es, int comp_mask, int64_t raw_cap,
                                int64_t c4_cap, int64_t c128_cap,
                                const int32_t* __restrict__ accept_len,
                                const int32_t* __restrict__ path_all, const char* treeK,
@@ -363,7 +363,7 @@ __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_
     if (ok) {
       for (int i = 0; i < n; ++i) {
         const int64_t src = ((int64_t)b * D + path[i]) * row_bytes;
-        const int64_t dst = ((int64_t)b * raw_cap + Lb + i) * row_bytes;
+        const int64_t dst = layer_row(pg, b, Lb + i, raw_cap, 1, status) * row_bytes;
         s_srcK[jobs] = treeK + src;
         s_srcV[jobs] = treeV + src;
         s_dstK[jobs] = rawK + dst;
@@ -371,7 +371,7 @@ __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_
         ++jobs;
         const int e = Lb + i;
         if ((comp_mask & TV_COMP_C4) && ((e + 1) & 3) == 0) {
-          const int64_t cd = ((int64_t)b * c4_cap + (e + 1) / 4 - 1) * row_bytes;
+          const int64_t cd = layer_row(pg, b, (e + 1) / 4 - 1, c4_cap, 4, status) * row_bytes;
           s_srcK[jobs] = scrK4 + src;
           s_srcV[jobs] = scrV4 + src;
           s_dstK[jobs] = c4K + cd;
@@ -379,7 +379,7 @@ __global__ void refresh_kernel(int D, int d, int es, int comp_mask, int64_t raw_
           ++jobs;
         }
         if ((comp_mask & TV_COMP_C128) && ((e + 1) & 127) == 0) {
-          const int64_t cd = ((int64_t)b * c128_cap + (e + 1) / 128 - 1) * row_bytes;
+          const int64_t cd = layer_row(pg, b, (e + 1) / 128 - 1, c128_cap, 128, status) * row_bytes;
           s_srcK[jobs] = scrK128 + src;
           s_srcV[jobs] = scrV128 + src;
           s_dstK[jobs] = c128K + cd;
@@ -424,14 +424,14 @@ static int launch_prefill_t(const tv_shape* s, const void* rawK, const void* raw
     const int64_t cap = s->c4_cap;
     const unsigned gx = (unsigned)(cap < 1 ? 1 : (cap > (1 << 20) ? (1 << 20) : cap));
     tv::prefill_kernel<T><<<dim3(gx, s->B), tv::kCompressThreads, 0, stream>>>(
-        4, d, s->raw_cap, cap, (const T*)rawK, (const T*)rawV, L, g4, (T*)c4K, (T*)c4V, status);
+        tv::paging_of(s), 4, d, s->raw_cap, cap, (const T*)rawK, (const T*)rawV, L, g4, (T*)c4K, (T*)c4V, status);
     if (int rc = tv_check_launch("tv_prefill_compress (C4)")) return rc;
   }
   if (s->comp_mask & TV_COMP_C128) {
     const int64_t cap = s->c128_cap;
     const unsigned gx = (unsigned)(cap < 1 ? 1 : (cap > (1 << 20) ? (1 << 20) : cap));
     tv::prefill_kernel<T><<<dim3(gx, s->B), tv::kCompressThreads, 0, stream>>>(
-        128, d, s->raw_cap, cap, (const T*)rawK, (const T*)rawV, L, g128, (T*)c128K,
+        tv::paging_of(s), 128, d, s->raw_cap, cap, (const T*)rawK, (const T*)rawV, L, g128, (T*)c128K,
         (T*)c128V, status);
     if (int rc = tv_check_launch("tv_prefill_compress (C128)")) return rc;
   }
@@ -457,13 +457,13 @@ int tv_launch_branch(const tv_shape* s, const void* rawK, const void* rawV, cons
   if (s->dtype == TV_BF16) {
     using T = __nv_bfloat16;
     tv::branch_kernel<T><<<grid, tv::kCompressThreads, 0, stream>>>(
-        s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
+        tv::paging_of(s), s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
         (const T*)treeK, (const T*)treeV, parents, g4, g128, (T*)scrK4, (T*)scrV4,
         (T*)scrK128, (T*)scrV128, status);
   } else {
     using T = float;
     tv::branch_kernel<T><<<grid, tv::kCompressThreads, 0, stream>>>(
-        s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
+        tv::paging_of(s), s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
         (const T*)treeK, (const T*)treeV, parents, g4, g128, (T*)scrK4, (T*)scrV4,
         (T*)scrK128, (T*)scrV128, status);
   }
@@ -477,7 +477,7 @@ int tv_launch_refresh(const tv_shape* s, const int32_t* accept_len, const int32_
                       int32_t* committed, int32_t* status, cudaStream_t stream) {
   const int es = s->dtype == TV_BF16 ? 2 : 4;
   tv::refresh_kernel<<<s->B, 256, 0, stream>>>(
-      s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap, accept_len, path,
+      tv::paging_of(s), s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap, accept_len, path,
       (const char*)treeK, (const char*)treeV, (const char*)scrK4, (const char*)scrV4,
       (const char*)scrK128, (const char*)scrV128, (char*)rawK, (char*)rawV, (char*)c4K,
       (char*)c4V, (char*)c128K, (char*)c128V, L, committed, status);

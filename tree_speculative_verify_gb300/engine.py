@@ -41,11 +41,12 @@ class DeviceState:
     c128V: torch.Tensor
     L: torch.Tensor
     k_idx: torch.Tensor = None    # [B][c4_cap][64] bf16 indexer keys (sparse C4 path only)
+    page_table: torch.Tensor = None   # [B][max_pages] int32 (paged pools only)
 
     def clone(self):
         return DeviceState(*(t.clone() for t in (self.rawK, self.rawV, self.c4K, self.c4V,
                                                  self.c128K, self.c128V, self.L)),
-                           k_idx=self.k_idx)
+                           k_idx=self.k_idx, page_table=self.page_table)
 
 
 @dataclass
@@ -90,6 +91,45 @@ def alloc_state(wl, device="cuda"):
         c128K=z(wl.cap128 if 128 in wl.ms else 0), c128V=z(wl.cap128 if 128 in wl.ms else 0),
         L=torch.as_tensor(wl.L, dtype=torch.int32).to(device),
         k_idx=None if wl.k_idx is None else wl.k_idx.to(device))
+
+
+def alloc_paged(wl, page_tokens, attn_kernel=_lib.TV_ATTN_AUTO, spare_pages=None, seed=0,
+                device="cuda"):
+    """Page-based persistent cache ("Adapting Tree-Structured Speculative Decoding to DeepSeek-V4
+    for Efficient Inference" §4.2: one logical layer, three physical layers with shared page
+    pointers).  Three pools of n_pool_pages pages -- raw K/V (P rows), C4 (P/4 entries), C128
+    (P/128 entries) -- and a page table [B][max_pages] mapping each request's logical page to one
+    pool page used by all three layers.  The pages of the batch are a seeded random permutation
+    of the pool (a fragmented pool), plus ``spare_pages`` unused ones.  Returns (shape, state); the
+    raw rows of the workload are copied into their pages, compressed entries start at zero."""
+    P = int(page_tokens)
+    max_pages = -(-wl.raw_cap // P)
+    spare = wl.B if spare_pages is None else int(spare_pages)
+    n_pool = wl.B * max_pages + spare
+    perm = torch.randperm(n_pool, generator=torch.Generator().manual_seed(seed))
+    table = perm[: wl.B * max_pages].reshape(wl.B, max_pages).to(torch.int32)
+    dt = wl.torch_dtype
+    z = lambda rows: torch.zeros((n_pool, max(rows, 1), wl.d), dtype=dt, device=device)
+    rawK, rawV = z(P), z(P)
+    for b in range(wl.B):
+        for g in range(max_pages):
+            lo, hi = g * P, min((g + 1) * P, wl.raw_cap)
+            if lo < hi:
+                rawK[int(table[b, g]), : hi - lo] = wl.rawK[b, lo:hi].to(device)
+                rawV[int(table[b, g]), : hi - lo] = wl.rawV[b, lo:hi].to(device)
+    k_idx = None
+    if wl.k_idx is not None:   # indexer keys stay contiguous, one row per logical C4 entry
+        k_idx = torch.zeros((wl.B, max_pages * P // 4, wl.k_idx.shape[2]), dtype=wl.k_idx.dtype,
+                            device=device)
+        k_idx[:, : wl.k_idx.shape[1]] = wl.k_idx.to(device)
+    st = DeviceState(rawK=rawK, rawV=rawV, c4K=z(P // 4), c4V=z(P // 4), c128K=z(P // 128),
+                     c128V=z(P // 128), L=torch.as_tensor(wl.L, dtype=torch.int32).to(device),
+                     k_idx=k_idx, page_table=table.to(device))
+    shape = shape_for(wl, attn_kernel)
+    shape.raw_cap, shape.c4_cap, shape.c128_cap = max_pages * P, max_pages * P // 4, max_pages * P // 128
+    shape.page_tokens, shape.max_pages, shape.n_pool_pages = P, max_pages, n_pool
+    shape.page_table = st.page_table.data_ptr()
+    return shape, st
 
 
 def alloc_round(wl, shape, device="cuda"):
