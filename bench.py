@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the budget sweep instead of the bench line: D x batch x {chain, tree} x "
                          "child-match probability at prefix 4096, one JSON line per cell")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="copy streams for the end-to-end uploads")
     ap.add_argument("--page-tokens", type=int, default=0,
                     help="keep the persistent cache in page pools of this many tokens per page "
                          "(a multiple of 512; pages scattered over the pool); 0 = contiguous")
@@ -492,30 +494,46 @@ def run_ours(args, world, rank, local):
                 for _ in range(n_sets)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
-    copy_stream = torch.cuda.Stream()
+    # uploads split over several copy streams (large inputs in slices along the batch), so that
+    # more than one copy engine moves the step's inputs
+    n_cs = max(1, args.copy_streams)
+    copy_streams = [torch.cuda.Stream() for _ in range(n_cs)]
     freed = [torch.cuda.Event() for _ in range(n_sets)]     # the set's last round has finished
-    landed = [torch.cuda.Event() for _ in range(n_sets)]    # the set's inputs are on the device
+    landed = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(n_sets)]
 
     def e2e_upload(i):
         s_, r_, _ = sets[i % n_sets]
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(freed[i % n_sets])
-            for dst, src in zip(in_tensors(r_), host_in):
-                dst.copy_(src, non_blocking=True)
-            landed[i % n_sets].record(copy_stream)
+        pieces = []
+        for dst, src in zip(in_tensors(r_), host_in):
+            if dst.numel() * dst.element_size() >= (4 << 20) and dst.shape[0] >= n_cs:
+                step_ = -(-dst.shape[0] // n_cs)
+                pieces += [(dst[k:k + step_], src[k:k + step_]) for k in range(0, dst.shape[0], step_)]
+            else:
+                pieces.append((dst, src))
+        for c, cs in enumerate(copy_streams):
+            with torch.cuda.stream(cs):
+                cs.wait_event(freed[i % n_sets])
+                for dst, src in pieces[c::n_cs]:
+                    dst.copy_(src, non_blocking=True)
+                landed[i % n_sets][c].record(cs)
 
     def e2e_round(i):
         s_, r_, l_ = sets[i % n_sets]
-        stream.wait_event(landed[i % n_sets])
-        s_.L.copy_(l_, non_blocking=True)
-        engine.verify_round(shape, s_, r_, None, stream, select=select)
+        for ev_ in landed[i % n_sets]:
+            stream.wait_event(ev_)
+        if graphs:
+            graphs[i % n_sets].replay()   # the captured round (its prologue resets L)
+        else:
+            s_.L.copy_(l_, non_blocking=True)
+            engine.verify_round(shape, s_, r_, None, stream, select=select)
         for dst, src in zip(host_out[i % n_sets], out_tensors(r_)):
             dst.copy_(src, non_blocking=True)
         freed[i % n_sets].record(stream)
 
     def e2e_run(n, t0=None):
         if t0 is not None:
-            copy_stream.wait_event(t0)
+            for cs in copy_streams:
+                cs.wait_event(t0)
         e2e_upload(0)
         for k in range(n):
             if k + 1 < n:
@@ -578,8 +596,10 @@ def run_ours(args, world, rank, local):
         "attention_ms": attn_ms,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "verified tree tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "note": "eager round through the C ABI; inputs uploaded from pinned host memory "
-                        "one step ahead on a copy stream; acceptance results read back each step"},
+                "note": ("the captured round (engine.RoundGraph)" if graphs else
+                         "the round launched call by call") + " through the C ABI; inputs "
+                        f"uploaded from pinned host memory one step ahead on {n_cs} copy "
+                        "stream(s); acceptance results read back each step"},
         "gpu_launches": args.steps * launches_per_step(shape, tc_name),
         "clocks": clk,
     }
