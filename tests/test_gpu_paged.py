@@ -48,6 +48,12 @@ CASES = {
     "short_prefixes_P512": (lambda: workloads.make_workload(
         "short", B=4, D=8, H=16, d=512, W=128, tail_mode="window", ms=(4, 128), dtype="bf16",
         L=(0, 130), k=2, steps=4, p_match=0.6, seed=5, kv_scale=0.5), 512, _lib.TV_ATTN_AUTO),
+    "remainder_tail_P512": (lambda: workloads.make_workload(
+        "rem", B=4, D=8, H=16, d=512, W=0, tail_mode="remainder", ms=(4,), dtype="bf16",
+        L=(97, 1203), k=2, steps=4, p_match=0.6, seed=13, kv_scale=0.5), 512, _lib.TV_ATTN_AUTO),
+    "d64_nodes_simt_P512": (lambda: workloads.make_workload(
+        "d64", B=2, D=64, H=2, d=512, W=128, tail_mode="window", ms=(4, 128), dtype="bf16",
+        L=(500, 700), k=2, steps=6, p_match=0.6, seed=11, kv_scale=0.5), 512, _lib.TV_ATTN_AUTO),
     "fp32_d64_P512": (lambda: workloads.make_workload(
         "f32", B=3, D=6, H=8, d=64, W=128, tail_mode="window", ms=(4, 128), dtype="f32",
         L=(200, 900), k=2, steps=3, p_match=0.6, seed=9, kv_scale=0.5), 512, _lib.TV_ATTN_AUTO),

@@ -235,13 +235,16 @@ class RoundGraph:
     "Adapting Tree-Structured Speculative Decoding to DeepSeek-V4 for Efficient Inference" §4.3
     replays the verification step as a CUDA graph sized for the tree configuration; here the five
     calls (and an optional ``prologue`` of stream work, e.g. refilling inputs) are captured once
-    and ``replay()`` relaunches them with a single graph launch.  The buffers in ``st`` / ``rb``
-    must stay allocated and at the same addresses; their contents may change between replays.
+    and ``replay()`` relaunches them with a single graph launch.  Construction runs one round
+    without its commit (outputs and scratch pad are overwritten, the persistent state is not).
+    The buffers in ``st`` / ``rb`` must stay allocated and at the same addresses; their contents
+    may change between replays.
     """
 
     def __init__(self, shape, st, rb, scale=None, commit=True, prologue=None, select=False):
-        # one eager round first: per-device set-up of the library happens outside the capture
-        verify_round(shape, st, rb, scale, None, commit, select)
+        # one eager round first, without the commit (the persistent state is left as it was):
+        # the library's once-per-device set-up happens outside the capture
+        verify_round(shape, st, rb, scale, None, False, select)
         torch.cuda.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
