@@ -69,6 +69,25 @@ def test_sweep_cells(idx):
     _run(wl)
 
 
+def _serving_like(name, B, L, seed):
+    return workloads.make_workload(name, B=B, D=8, H=64, d=512, W=128, tail_mode="window",
+                                   ms=(4, 128), dtype="bf16", L=L, k=2, steps=4, p_match=0.55,
+                                   seed=seed, kv_scale=0.5)
+
+
+def test_more_work_items_than_cta_pairs():
+    # 48 requests x 2 row-tile pairs x 2 value halves = 192 work items of ragged sizes: more than
+    # the CTA pairs that fit on the device at once, so later items start as earlier ones finish
+    _run(_serving_like("many_items", 48, (200, 900), 22))
+
+
+def test_split_kv_with_empty_chunks():
+    # 12 requests up to 8191 tokens: the KV tiles are split into chunks (fp32 partials + merge),
+    # 144 work items; the nearly empty requests (L = 0, 1, 3) leave later chunks without a tile
+    Ls = [8000, 0, 7000, 3, 8100, 64, 7900, 129, 6000, 1, 8191, 500]
+    _run(_serving_like("split_items", 12, Ls, 21))
+
+
 # --- edge cases ------------------------------------------------------------------------------
 
 def _edge(name, **kw):

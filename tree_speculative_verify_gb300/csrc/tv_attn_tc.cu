@@ -23,7 +23,8 @@
 // mask, scratch visibility) inside the softmax warps.
 //
 // Warp roles (352 threads per CTA):
-//   warp 0      TMA producer: Q once (8 boxes of 128 x 64); then, through a 3-slot ring of 32 KB,
+//   warp 0      TMA producer: Q once (8 boxes of 128 x 64, completing on the leader's barrier like
+//               every other copy of the pair); then, through a 3-slot ring of 32 KB,
 //               this CTA's share of every tile: for S, two slots of four 64-dim slices of N/2
 //               entries; for PV, one slot of the tile's entries x 128 value columns
 //   warp 1      both CTAs: allocate / free 512 TMEM columns (cta_group::2).  Leader lane 0 issues
@@ -248,7 +249,7 @@ struct __align__(1024) Smem {
   uint8_t ring[kSlots][kSlotBytes];
   uint64_t full[kSlots];       // (leader) both CTAs' shares of a fill have landed
   uint64_t empty[kSlots];      // the pair's MMAs are done with the slot
-  uint64_t q_full;
+  uint64_t q_full;             // (leader) both CTAs' Q rows have landed
   uint64_t s_full[2];
   uint64_t p_full[2];          // (leader) P written by both CTAs' softmax warps: the leader's
                                // arrive with expect_tx(4) + the follower's 4-byte st.async
@@ -297,9 +298,11 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
     issued_phase[i] = 0;
   }
   if (lane == 0) {
-    mbar_arrive_expect_tx(&sm.q_full, kQBytes);
+    // both CTAs' Q rows complete on the leader's q_full: the pair's MMAs read both
+    const uint32_t q_bar = mapa_cluster(smem_u32(&sm.q_full), 0);
+    if (rank == 0) mbar_arrive_expect_tx(&sm.q_full, 2 * kQBytes);
     for (int s = 0; s < 8; ++s)
-      tma_load_3d(sm.q + s * 16384, &p.mQ, 64 * s, 128 * rt, b, &sm.q_full);
+      tma_load_3d_pair(sm.q + s * 16384, &p.mQ, 64 * s, 128 * rt, b, q_bar);
   }
   auto acquire = [&]() -> bool {
     if (!mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort, kTimeoutNs)) {
@@ -418,15 +421,14 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
   }
   if (ok && te > tb) load_v(tile_of(y, te - 1), prev);
   // drain: no copy issued by the pair may still be in flight when the CTA exits (the leader's
-  // full barriers count both CTAs' shares; the closing cluster barrier covers the follower)
-  if (rank == 0)
+  // full and q_full barriers count both CTAs' shares; the closing cluster barrier covers the
+  // follower)
+  if (rank == 0) {
+    volatile int never = 0;
     for (int i = 0; i < kSlots; ++i)
-      if (issued[i]) {
-        volatile int never = 0;
-        mbar_wait(&sm.full[i], issued_phase[i], &never, kTimeoutNs / 4);
-      }
-  volatile int never = 0;
-  mbar_wait(&sm.q_full, 0, &never, kTimeoutNs / 4);
+      if (issued[i]) mbar_wait(&sm.full[i], issued_phase[i], &never, kTimeoutNs / 4);
+    mbar_wait(&sm.q_full, 0, &never, kTimeoutNs / 4);
+  }
 }
 
 // ---- leader lane 0 of warp 1: the pair's MMAs ---------------------------------------------------
@@ -638,21 +640,22 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
         break;
       }
       tc_fence_after();
-      for (int c = 0; c < kOColsPerThread / 32; ++c) {
-        uint32_t r[32];
-        const uint32_t col = tmem + lane_base + 256 + kOColsPerThread * ch + 32 * c;
-        tmem_ld32(col, r);
+#pragma unroll 1
+      for (int c = 0; c < kOColsPerThread / 8; ++c) {
+        uint32_t r[8];
+        const uint32_t col = tmem + lane_base + 256 + kOColsPerThread * ch + 8 * c;
+        tmem_ld8(col, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-        tmem_st32(col, r);
+        for (int k = 0; k < 8; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+        tmem_st8(col, r);
       }
       tmem_wait_st();
     }
     const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
-    float sum[8];
+    float sum[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sum[k] = 0.f;
+    for (int k = 0; k < 4; ++k) sum[k] = 0.f;
 #pragma unroll
     for (int c = 0; c < kColsPerThread / 64; ++c) {
       uint32_t pk[32];
@@ -660,15 +663,14 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
       for (int j = 0; j < 32; ++j) {
         const float p0 = ex2_approx(fmaf(s[64 * c + 2 * j], sl2, neg_m));
         const float p1 = ex2_approx(fmaf(s[64 * c + 2 * j + 1], sl2, neg_m));
-        sum[j & 7] += p0 + p1;
+        sum[j & 3] += p0 + p1;
         const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
         pk[j] = *reinterpret_cast<const uint32_t*>(&h);
       }
       // P column k holds entries 2k and 2k+1
       if (c0 + 64 * c < x.nqk) tmem_st32(tmem + lane_base + 128 * sb + (c0 >> 1) + 32 * c, pk);
     }
-    const float tsum =
-        ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+    const float tsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     l_run = l_run * alpha + tsum;
     m_ref = m_new;
     tmem_wait_st();

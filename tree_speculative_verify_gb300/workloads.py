@@ -177,10 +177,14 @@ def _caps(L_max, D):
 
 def make_workload(name, *, B, D, H, d, W, tail_mode, ms, dtype, L, k, steps, p_match, seed,
                   kv_scale, n_sel=0, forced=None, fixed_parents=None, beam=False):
-    """Draw one workload.  ``L`` is an int (same for all requests) or a (lo, hi) uniform range."""
+    """Draw one workload.  ``L`` is an int (same for all requests), a (lo, hi) uniform range or a
+    list of B lengths."""
     rng = np.random.Generator(np.random.PCG64(seed))
     if isinstance(L, tuple):
         Ls = rng.integers(L[0], L[1] + 1, size=B).astype(np.int64)
+    elif isinstance(L, list):
+        assert len(L) == B, "one length per request"
+        Ls = np.asarray(L, dtype=np.int64)
     else:
         Ls = np.full(B, int(L), dtype=np.int64)
     parents = np.empty((B, D), dtype=np.int32)
