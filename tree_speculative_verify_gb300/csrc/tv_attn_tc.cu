@@ -259,6 +259,7 @@ struct __align__(1024) Smem {
   uint64_t o_full;
   uint64_t drain;
   float xmax[2][2][128];       // [tile parity][column half][row] partial row maxima
+  int xok[2][2][4];            // [tile parity][column half][lane quadrant] the warp carries on
   uint32_t tmem;
   int abort;
 };
@@ -579,54 +580,67 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
 
   float m_ref = -INFINITY, l_run = 0.f;
   const int n = te - tb;
+  // The two warps of a row (column halves) meet at one named barrier per tile and one after the
+  // tiles.  A warp whose bounded wait ran out still takes each barrier until both warps leave the
+  // tile loop together (each tile's exchange carries both warps' flags), so neither waits on the
+  // other forever.
   bool ok = true;
-  for (int i = 0; i < n && ok; ++i) {
+  for (int i = 0; i < n; ++i) {
     const Tile x = tile_of(y, tb + i);
     const int sb = i & 1;
     const int c0 = kColsPerThread * ch;     // first S column of this thread
     // the wait result is made warp-uniform: tcgen05.ld below is warp-collective
-    if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs))) {
+    if (ok && !__all_sync(0xffffffffu,
+                          mbar_wait(&sm.s_full[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs))) {
       fail(sm, p.status);
       ok = false;
-      break;
     }
-    tc_fence_after();
     float s[kColsPerThread];
-    {
-      uint32_t* sr = reinterpret_cast<uint32_t*>(s);
+    float raw_max = -INFINITY;
+    if (ok) {
+      tc_fence_after();
+      {
+        uint32_t* sr = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-      for (int c = 0; c < kColsPerThread / 32; ++c)
-        if (c0 + 32 * c < x.nqk)
-          tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32 * c,
-                    *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-      tmem_wait_ld();
-    }
-    // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
-    float mx[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-    const bool full_tile = (x.kind == kC4 || x.kind == kC128) && x.valid >= 128;
-    if (full_tile) {
-#pragma unroll
-      for (int j = 0; j < kColsPerThread; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < kColsPerThread; ++j) {
-        const int col = c0 + j;
-        bool vis = col < x.valid;
-        if (x.kind == kRaw) vis = vis && (x.row0 + col >= raw_lo);
-        if (x.kind == kExtra) vis = col < 32 && ((extra_mask >> (col & 31)) & 1u);
-        s[j] = vis ? s[j] : -INFINITY;
-        mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+        for (int c = 0; c < kColsPerThread / 32; ++c)
+          if (c0 + 32 * c < x.nqk)
+            tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32 * c,
+                      *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+        tmem_wait_ld();
       }
+      // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+      const bool full_tile = (x.kind == kC4 || x.kind == kC128) && x.valid >= 128;
+      if (full_tile) {
+#pragma unroll
+        for (int j = 0; j < kColsPerThread; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kColsPerThread; ++j) {
+          const int col = c0 + j;
+          bool vis = col < x.valid;
+          if (x.kind == kRaw) vis = vis && (x.row0 + col >= raw_lo);
+          if (x.kind == kExtra) vis = col < 32 && ((extra_mask >> (col & 31)) & 1u);
+          s[j] = vis ? s[j] : -INFINITY;
+          mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+        }
+      }
+      raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
     }
-    float raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
     if (kCh == 2) {
       sm.xmax[sb][ch][row] = raw_max;
+      if (lane == 0) sm.xok[sb][ch][quad] = ok ? 1 : 0;
       pair_sync(quad);
       raw_max = fmaxf(raw_max, sm.xmax[sb][ch ^ 1][row]);
+      if (ok && !sm.xok[sb][ch ^ 1][quad]) {   // the row's other warp gave up
+        fail(sm, p.status);
+        ok = false;
+      }
     }
+    if (!ok) break;
     const float mt = raw_max * sl2;
     const bool grow_max = mt > m_ref + kRescaleThreshold;
     const float m_new = grow_max ? mt : m_ref;
@@ -636,8 +650,8 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
     if (__any_sync(0xffffffffu, need_rescale)) {
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (i - 1) & 1, &sm.abort, kTimeoutNs))) {
         fail(sm, p.status);
-        ok = false;
-        break;
+        ok = false;   // the tile loop ends at the next exchange, together with the other warp
+        continue;
       }
       tc_fence_after();
 #pragma unroll 1
