@@ -66,6 +66,27 @@ def test_exact_ties_go_to_the_lower_index():
         assert np.array_equal(got[b], want), f"request {b}"
 
 
+def test_more_entries_than_shared_memory_holds():
+    # 42500 C4 entries: above the 40960 keys the select kernel stages, so every pass re-reads the
+    # scores from global memory
+    wl = workloads.long_context(B=1, L=(170000, 170000), n_sel=2048)
+    got, status = _gpu_select(wl)
+    assert status == 0
+    assert np.array_equal(got[0], _oracle_select(wl, 0))
+
+
+def test_all_scores_equal():
+    # a zero query: every score is 0, all keys tie, the lowest n_sel indices are kept
+    wl = workloads.long_context(B=2, L=(3000, 5000), n_sel=300)
+    wl.q_idx = torch.zeros_like(wl.q_idx)
+    got, status = _gpu_select(wl)
+    assert status == 0
+    for b in range(2):
+        want = _oracle_select(wl, b)
+        assert np.array_equal(want, np.arange(300))
+        assert np.array_equal(got[b], want), f"request {b}"
+
+
 def test_too_few_entries_is_reported_per_request():
     wl = workloads.long_context(B=3, L=(3000, 3100), n_sel=64)
     L = wl.L.copy()

@@ -65,38 +65,22 @@ __global__ void score_kernel(int B, int64_t c4_cap, int d_idx, const uint16_t* _
   score[t] = s;
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int n_sel,
-                                                             const int32_t* __restrict__ L,
-                                                             const float* __restrict__ score,
-                                                             int32_t* __restrict__ sel,
-                                                             int32_t* status) {
-  extern __shared__ uint32_t keys_smem[];
-  __shared__ unsigned hist[256];
-  __shared__ int warp_gt[32], warp_eq[32];
-  __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_krem;
-  const int b = blockIdx.x;
+// The radix select and the ordered write for one request of n4 keys.  kStaged: the keys are in
+// shared memory (read four at a time in the histogram passes); otherwise each pass re-reads the
+// scores.  The shared-memory arrays come from the kernel.
+template <bool kStaged>
+__device__ __forceinline__ void select_request(int n4, int n_sel, const uint32_t* keys_smem,
+                                               const float* __restrict__ sc,
+                                               int32_t* __restrict__ out, unsigned* hist,
+                                               int* warp_gt, int* warp_eq, uint32_t* s_prefix,
+                                               uint32_t* s_mask, int* s_krem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int Lb = L[b];
-  const int64_t n4 = Lb >= 0 ? Lb / 4 : -1;
-  int32_t* out = sel + (int64_t)b * n_sel;
-  if (n4 < n_sel || n4 > c4_cap) {
-    if (threadIdx.x == 0) record_error(status, n4 > c4_cap ? TV_ERR_CAPACITY : TV_ERR_SELECTION);
-    for (int i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = -1;
-    return;
-  }
-  const float* sc = score + (int64_t)b * c4_cap;
-  const bool staged = n4 <= kSmemKeys;
-  if (staged) {
-#pragma unroll 8
-    for (int64_t j = threadIdx.x; j < n4; j += blockDim.x) keys_smem[j] = score_key(sc[j]);
-  }
-  auto key_at = [&](int64_t j) -> uint32_t { return staged ? keys_smem[j] : score_key(sc[j]); };
+  auto key_at = [&](int j) -> uint32_t { return kStaged ? keys_smem[j] : score_key(sc[j]); };
   if (threadIdx.x == 0) {
-    s_prefix = 0u;
-    s_mask = 0u;
-    s_krem = n_sel;
+    *s_prefix = 0u;
+    *s_mask = 0u;
+    *s_krem = n_sel;
   }
   __syncthreads();
   // radix select of the n_sel-th largest key, most significant digit first (shared-memory atomics
@@ -104,21 +88,30 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
     __syncthreads();
-    const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int64_t j0 = 0; j0 < n4; j0 += blockDim.x) {
-      const int64_t j = j0 + threadIdx.x;
-      int bin = -1;
-      if (j < n4) {
-        const uint32_t key = key_at(j);
-        if ((key & mask) == prefix) bin = (int)((key >> shift) & 255u);
+    const uint32_t prefix = *s_prefix, mask = *s_mask;
+    auto count = [&](uint32_t key) {
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    };
+    if (kStaged) {
+      // four keys per 16-byte load; keys past n4 in the last vector are not counted
+      const uint4* k4 = reinterpret_cast<const uint4*>(keys_smem);
+      const int n16 = (n4 + 3) >> 2;
+      for (int q = threadIdx.x; q < n16; q += blockDim.x) {
+        const uint4 v = k4[q];
+        const int j = 4 * q;
+        count(v.x);
+        if (j + 1 < n4) count(v.y);
+        if (j + 2 < n4) count(v.z);
+        if (j + 3 < n4) count(v.w);
       }
-      if (bin >= 0) atomicAdd(&hist[bin], 1u);
+    } else {
+      for (int j = threadIdx.x; j < n4; j += blockDim.x) count(score_key(sc[j]));
     }
     __syncthreads();
     if (warp == 0) {
       // lane l holds bins 255-8l .. 248-8l (descending); an inclusive scan over lanes gives the
       // count of keys in the digits above each lane's group
-      const int krem = s_krem;
+      const int krem = *s_krem;
       int c[8], sum = 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -142,23 +135,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
           }
           above += c[q];
         }
-        s_krem = krem - above;
-        s_prefix = prefix | ((uint32_t)digit << shift);
-        s_mask = mask | (255u << shift);
+        *s_krem = krem - above;
+        *s_prefix = prefix | ((uint32_t)digit << shift);
+        *s_mask = mask | (255u << shift);
       }
     }
     __syncthreads();
   }
-  const uint32_t T = s_prefix;   // key of the n_sel-th best entry
-  const int need_eq = s_krem;    // entries with key == T to keep: the lowest-indexed ones
+  const uint32_t T = *s_prefix;   // key of the n_sel-th best entry
+  const int need_eq = *s_krem;    // entries with key == T to keep: the lowest-indexed ones
   // warp w owns the contiguous index range [w * R, (w + 1) * R), read 32 consecutive keys at a
   // time: count, one scan over the warps, then write the kept entries in ascending order
   const int n_warps = blockDim.x >> 5;
-  const int64_t R = (n4 + n_warps - 1) / n_warps;
-  const int64_t lo = warp * R, hi = lo + R < n4 ? lo + R : n4;
+  const int R = (n4 + n_warps - 1) / n_warps;
+  const int lo = warp * R, hi = lo + R < n4 ? lo + R : n4;
   int gt = 0, eq = 0;
-  for (int64_t j0 = lo; j0 < hi; j0 += 32) {
-    const int64_t j = j0 + lane;
+  for (int j0 = lo; j0 < hi; j0 += 32) {
+    const int j = j0 + lane;
     const uint32_t key = j < hi ? key_at(j) : 0u;
     gt += __popc(__ballot_sync(0xffffffffu, j < hi && key > T));
     eq += __popc(__ballot_sync(0xffffffffu, j < hi && key == T));
@@ -175,16 +168,49 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
   }
   int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
   int eq_seen = eq_before;
-  for (int64_t j0 = lo; j0 < hi; j0 += 32) {
-    const int64_t j = j0 + lane;
+  for (int j0 = lo; j0 < hi; j0 += 32) {
+    const int j = j0 + lane;
     const uint32_t key = j < hi ? key_at(j) : 0u;
     const bool is_gt = j < hi && key > T, is_eq = j < hi && key == T;
     const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
     const bool take = is_gt || (is_eq && eq_seen + __popc(eqm & lt_mask) < need_eq);
     const unsigned tm = __ballot_sync(0xffffffffu, take);
-    if (take) out[pos + __popc(tm & lt_mask)] = (int32_t)j;
+    if (take) out[pos + __popc(tm & lt_mask)] = j;
     pos += __popc(tm);
     eq_seen += __popc(eqm);
+  }
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int n_sel,
+                                                             const int32_t* __restrict__ L,
+                                                             const float* __restrict__ score,
+                                                             int32_t* __restrict__ sel,
+                                                             int32_t* status) {
+  extern __shared__ __align__(16) uint32_t keys_smem[];
+  __shared__ unsigned hist[256];
+  __shared__ int warp_gt[32], warp_eq[32];
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_krem;
+  const int b = blockIdx.x;
+  const int Lb = L[b];
+  const int64_t n4 = Lb >= 0 ? Lb / 4 : -1;
+  int32_t* out = sel + (int64_t)b * n_sel;
+  if (n4 < n_sel || n4 > c4_cap) {
+    if (threadIdx.x == 0) record_error(status, n4 > c4_cap ? TV_ERR_CAPACITY : TV_ERR_SELECTION);
+    for (int i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = -1;
+    return;
+  }
+  // n4 < 2^31: the shape check bounds B * c4_cap
+  const float* sc = score + (int64_t)b * c4_cap;
+  if (n4 <= kSmemKeys) {
+#pragma unroll 8
+    for (int j = threadIdx.x; j < (int)n4; j += blockDim.x) keys_smem[j] = score_key(sc[j]);
+    if (threadIdx.x < (unsigned)((-n4) & 3)) keys_smem[n4 + threadIdx.x] = 0u;   // whole vectors
+    select_request<true>((int)n4, n_sel, keys_smem, sc, out, hist, warp_gt, warp_eq, &s_prefix,
+                         &s_mask, &s_krem);
+  } else {
+    select_request<false>((int)n4, n_sel, keys_smem, sc, out, hist, warp_gt, warp_eq, &s_prefix,
+                          &s_mask, &s_krem);
   }
 }
 
@@ -204,8 +230,9 @@ int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const voi
   }
   // shared memory for the staged keys, sized by the capacity (requests with more entries than
   // kSmemKeys read the scores from global memory instead)
+  // (rounded up to whole 16-byte vectors: the histogram passes read four keys at a time)
   const int64_t staged = s->c4_cap < tv::kSmemKeys ? s->c4_cap : tv::kSmemKeys;
-  const size_t smem = (size_t)staged * sizeof(uint32_t);
+  const size_t smem = (size_t)((staged + 3) / 4 * 4) * sizeof(uint32_t);
   // once per device (a plain host call that also stays out of any stream being captured)
   static std::mutex attr_mu;
   static bool attr_set[64] = {};
