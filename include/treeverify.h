@@ -195,8 +195,10 @@ int tv_branch_compress(const tv_shape* shape, const void* rawK, const void* rawV
  *   Q    [B][D][H][d] in (dtype);  sel [B][n_sel] int32 (nullable when n_sel == 0)
  *   anc, raw_lo, scr_vis4, scr_vis128: the plan of tv_build_ancestor_mask
  *   O    [B][D][H][d] out (dtype); lse [B][D][H] fp32 out: natural-log sum of exp(logits)
+ *   (Q and O 16-byte aligned)
  *   workspace: device buffer of ws_bytes >= tv_workspace_size(shape)
- * Host errors: TV_ERR_WORKSPACE, TV_ERR_DTYPE (TV_ATTN_TCGEN05 asked for an unsupported shape).
+ * Host errors: TV_ERR_ARG (also a misaligned Q or O), TV_ERR_WORKSPACE, TV_ERR_DTYPE
+ * (TV_ATTN_TCGEN05 asked for an unsupported shape).
  * Device errors: TV_ERR_SELECTION, TV_ERR_CAPACITY, TV_ERR_TIMEOUT.
  */
 int tv_tree_verify_attn(const tv_shape* shape, const void* Q, const void* c4K, const void* c4V,

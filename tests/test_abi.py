@@ -86,6 +86,22 @@ def test_null_pointers_rejected_before_any_launch(lib):
     assert rc == -1
 
 
+def test_misaligned_q_or_o_rejected_before_any_launch(lib):
+    # stand-in device addresses: validation returns before anything touches them
+    s = _shape()
+    ok = ctypes.c_void_p(1 << 20)
+    ws_bytes = lib.tv_workspace_size(ctypes.byref(s))
+
+    def call(Q, O):
+        return lib.tv_tree_verify_attn(ctypes.byref(s), Q, *([ok] * 18), ctypes.c_float(0.05), O,
+                                       ok, ok, ws_bytes, ok, None)
+
+    rc = call(ok, ctypes.c_void_p((1 << 20) + 8))
+    assert rc == -1 and b"16-byte aligned" in lib.tv_last_error_string()
+    rc = call(ctypes.c_void_p((1 << 20) + 2), ok)
+    assert rc == -1 and b"16-byte aligned" in lib.tv_last_error_string()
+
+
 def test_empty_batch_is_a_no_op(lib):
     s = _shape(B=0)
     assert lib.tv_accept_walk(ctypes.byref(s), None, None, None, None, None, None, None, None) == 0

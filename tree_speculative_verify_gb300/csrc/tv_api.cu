@@ -358,6 +358,9 @@ extern "C" int tv_tree_verify_attn(const tv_shape* s, const void* Q, const void*
     return tv_set_error(TV_ERR_ARG, "%s: scale must be a positive finite number", fn);
   if (((uintptr_t)workspace) % 256 != 0)
     return tv_set_error(TV_ERR_ARG, "%s: workspace must be 256-byte aligned", fn);
+  // rows of Q and O are read and written 16 bytes at a time
+  if (((uintptr_t)Q | (uintptr_t)O) & 15u)
+    return tv_set_error(TV_ERR_ARG, "%s: Q and O must be 16-byte aligned", fn);
   const size_t need = tv_workspace_size(s);
   if (ws_bytes < need)
     return tv_set_error(TV_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, ws_bytes,

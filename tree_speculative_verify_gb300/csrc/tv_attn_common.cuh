@@ -196,15 +196,18 @@ __device__ __forceinline__ bool entry_visible(const EntryRef& r, const NodeVis& 
   return entry_visible_kind(r.kind, r.aux, n);
 }
 
-// Split-KV merge: one block per (request, node, head) row, d/4 threads; thread t owns columns
-// 4t .. 4t+3.  Every thread derives the chunk weights itself (a few dozen broadcast loads), so
-// the column loads of all chunks are independent and the row needs no block synchronisation.
+// Split-KV merge: a warp per (request, node, head) row, 8 rows per block; lane l owns columns
+// 4l .. 4l+3 of every 128-column group and writes them with one store.  Every lane derives the
+// chunk weights itself (a few dozen broadcast loads), so the column loads of all chunks are
+// independent and the row needs no synchronisation.
 // Chunk rows are d + 4 floats (16-byte aligned for d a multiple of 8): O partial, m (log2
 // units), l.
 template <typename T>
 __global__ void merge_kernel(int rows, int d, int n_chunks, const float* __restrict__ part,
                              T* __restrict__ O, float* __restrict__ lse) {
-  const int row = blockIdx.x;
+  // a warp per row: lane l combines columns 4l .. 4l+3 of every 128-column group
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int64_t stride = d + 4;
   const float* pr = part + (int64_t)row * n_chunks * stride;
@@ -215,7 +218,7 @@ __global__ void merge_kernel(int rows, int d, int n_chunks, const float* __restr
   for (int c = 0; c < n_chunks; ++c)
     if (pr[c * stride + d + 1] > 0.f) denom += exp2f(pr[c * stride + d] - M) * pr[c * stride + d + 1];
   const float inv = denom > 0.f ? 1.f / denom : 0.f;
-  for (int i = 4 * threadIdx.x; i < d; i += 4 * blockDim.x) {
+  for (int i = 4 * lane; i < d; i += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = 0; c < n_chunks; ++c) {
       const float* pc = pr + c * stride;
@@ -228,13 +231,10 @@ __global__ void merge_kernel(int rows, int d, int n_chunks, const float* __restr
         acc.w += w * v.w;
       }
     }
-    T* o = O + (int64_t)row * d + i;
-    store_f(o, acc.x * inv);
-    store_f(o + 1, acc.y * inv);
-    store_f(o + 2, acc.z * inv);
-    store_f(o + 3, acc.w * inv);
+    store_f4(O + (int64_t)row * d + i,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   }
-  if (threadIdx.x == 0)
+  if (lane == 0)
     lse[row] = denom > 0.f ? (M + log2f(denom)) * 0.6931471805599453f : -INFINITY;
 }
 
@@ -244,8 +244,9 @@ template <typename T>
 int tv_launch_merge(int B, int DH, int d, int n_chunks, const float* part, T* O, float* lse,
                     cudaStream_t stream) {
   const int rows = B * DH;
-  const int threads = d / 4 < 32 ? 32 : (d / 4 > 256 ? 256 : d / 4);
-  tv::merge_kernel<T><<<rows, threads, 0, stream>>>(rows, d, n_chunks, part, O, lse);
+  const int rows_per_block = 8;   // 256 threads, a warp per row
+  tv::merge_kernel<T><<<(rows + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0,
+                         stream>>>(rows, d, n_chunks, part, O, lse);
   return tv_check_launch("tv_tree_verify_attn (merge)");
 }
 
