@@ -92,3 +92,21 @@ def test_vectorised_blocks_equal_per_block_definition(m):
         np.testing.assert_allclose(CV[j], cv, atol=1e-14)
     CK2, _ = compress_blocks(rawK, rawV, 1, L // m, m, g, "f64")
     np.testing.assert_allclose(CK2, CK[1:], atol=1e-14)
+
+
+def test_many_blocks_span_several_slabs():
+    # 9000 C4 entries: the compressor widens the raw rows slab by slab (4096 entries per slab);
+    # entries at the slab edges, and a range that starts past entry 0, equal the closed form of
+    # their own block
+    rng = np.random.default_rng(21)
+    m, d, n = 4, 4, 9000
+    rawK = rng.standard_normal((m * n, d))
+    rawV = rng.standard_normal((m * n, d))
+    g = rng.standard_normal(d)
+    CK, CV = compress_prefix(rawK, rawV, m * n, m, g, "f64")
+    for j in (0, 1, 4095, 4096, 4097, 8191, 8192, 8999):
+        ck, cv, _ = _closed_form(rawK[m * j:m * j + m], rawV[m * j:m * j + m], g)
+        np.testing.assert_allclose(CK[j], ck, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(CV[j], cv, rtol=0, atol=1e-12)
+    CK2, CV2 = compress_blocks(rawK, rawV, 100, n, m, g, "f64")
+    assert np.array_equal(CK2, CK[100:]) and np.array_equal(CV2, CV[100:])
