@@ -155,13 +155,13 @@ def test_two_rounds_in_a_row():
         L0, L1 = int(wl.L[b]), res[b]["L_new"]
         wl2.rawK[b, L0:L1] = torch.from_numpy(res[b]["raw_rows"][0]).to(wl.rawK.dtype)
         wl2.rawV[b, L0:L1] = torch.from_numpy(res[b]["raw_rows"][1]).to(wl.rawV.dtype)
-    # the oracle state for round 2: its own committed entries on top of its prefix
+    # the oracle state for the second verify round: its own committed entries on top of its prefix
     comp2 = {m: (comp[m][0].copy(), comp[m][1].copy()) for m in comp}
     for b in range(wl.B):
         for (m, j), (ck, cv) in res[b]["entries"].items():
             comp2[m][0][b, j] = ck
             comp2[m][1][b, j] = cv
-    # raw rows committed by round 1 are bit-equal on both sides (checked above)
+    # raw rows committed by the first verify round are bit-equal on both sides (checked above)
     res2 = run_oracle(wl2, comp2)
     from tree_speculative_verify_gb300 import engine
     rb2 = engine.alloc_round(wl2, shape)
