@@ -20,6 +20,7 @@ import oracle.compress
 import oracle.indexer
 import oracle.plan
 import oracle.refresh
+import oracle.round
 import oracle.storage
 import oracle.verify
 import test_oracle_accept as p_accept
@@ -110,6 +111,12 @@ def _refresh():
         p_refresh.test_capacity_is_enforced, p_refresh.test_tiny_round_golden]
 
 
+def _round():
+    return [p_refresh.test_tiny_round_golden] + [
+        lambda L=L: p_refresh.test_round_reports_the_rows_and_entries_it_commits(L)
+        for L in (250, 253)]
+
+
 def _indexer():
     return [p_indexer.test_integer_scores_equal_the_exact_dot_product,
             p_indexer.test_scores_round_in_index_order,
@@ -124,8 +131,8 @@ def _storage():
             p_storage.test_f32_matches_exact_rational, p_storage.test_f64_is_identity]
 
 
-C, P, V, A, R, I, S = (oracle.compress, oracle.plan, oracle.verify, oracle.accept, oracle.refresh,
-                       oracle.indexer, oracle.storage)
+C, P, V, A, R, I, S, RD = (oracle.compress, oracle.plan, oracle.verify, oracle.accept,
+                           oracle.refresh, oracle.indexer, oracle.storage, oracle.round)
 
 MUTANTS = [
     # compressor ([TSD-V4] §2.2, the gated-sum stand-in)
@@ -180,6 +187,15 @@ MUTANTS = [
      "rawK[L + i] = to_f64(treeK[i])", _refresh),
     ("entry index one high", R.refresh_commit_request, "j = (e + 1) // m - 1", "j = (e + 1) // m",
      _refresh),
+    # the round: the steps in order, per request ([TSD-V4] §4.1, §4.4)
+    ("walk given draft and target swapped", RD.verify_round,
+     "accept_walk(par, draft[b], target[b])", "accept_walk(par, target[b], draft[b])", _round),
+    ("reported entry one block high", RD.verify_round, "                        j = (e + 1) // m - 1",
+     "                        j = (e + 1) // m", _round),
+    ("reported raw rows shifted", RD.verify_round, "raw_rows=(rK[Lb:L_new].copy(), rV[Lb:L_new].copy())",
+     "raw_rows=(rK[Lb - 1:L_new - 1].copy(), rV[Lb - 1:L_new - 1].copy())", _round),
+    ("another request's tree", RD.verify_round, "par = [int(x) for x in parents[b]]",
+     "par = [int(x) for x in parents[0]]", _round),
     # indexer (the sparse C4 path)
     ("ties to the higher index", I.topk_ascending, "key=lambda j: (-float(scores[j]), j)",
      "key=lambda j: (-float(scores[j]), -j)", _indexer),

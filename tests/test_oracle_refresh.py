@@ -82,3 +82,49 @@ def test_tiny_round_golden():
     assert res["committed"].tolist() == gold["committed_pos"]
     assert res["scratch"] == {}          # L = 256 and depth <= 2: no node closes a 4-block
     assert res["entries"] == {}
+
+
+@pytest.mark.parametrize("L", [250, 253])
+def test_round_reports_the_rows_and_entries_it_commits(L):
+    # a 2-request round over two different branching trees: what the round reports as written
+    # (raw rows, compressed entries, new length) equals rebuilding prefix + accepted path from
+    # scratch, each request with its own tree and tokens
+    rng = np.random.default_rng(L)
+    B, D, d, H, W, ms = 2, 7, 8, 2, 6, (4, 128)
+    parents = np.array([[-1, 0, 0, 1, 1, 3, 4], [-1, 0, 1, 1, 2, 0, 5]])
+    cap = L + D + 4
+    rawK = np.zeros((B, cap, d))
+    rawV = np.zeros((B, cap, d))
+    rawK[:, :L] = rng.standard_normal((B, L, d))
+    rawV[:, :L] = rng.standard_normal((B, L, d))
+    treeK = rng.standard_normal((B, D, d))
+    treeV = rng.standard_normal((B, D, d))
+    Q = rng.standard_normal((B, D, H, d))
+    g = {m: rng.standard_normal(d) for m in ms}
+    comp = {}
+    for m in ms:
+        ck = np.zeros((B, cap // m + 1, d))
+        cv = np.zeros((B, cap // m + 1, d))
+        for b in range(B):
+            ck[b, :L // m], cv[b, :L // m] = compress_prefix(rawK[b], rawV[b], L, m, g[m], "f64")
+        comp[m] = (ck, cv)
+    draft = np.array([[9, 1, 2, 3, 4, 5, 6]] * B)
+    # request 0 accepts 0 -> 1 -> 3 -> 5 (bonus 40); request 1 accepts 0 -> 5 -> 6 (bonus 42)
+    target = np.array([[1, 3, 41, 5, 0, 40, 0], [5, 0, 0, 0, 0, 6, 42]])
+    cfg = VerifyConfig(H=H, d=d, ms=ms, W=W, tail_mode="window", store="f64")
+    res = verify_round(cfg, parents, np.array([L, L]), Q, comp, None, rawK, rawV, treeK, treeV, g,
+                       draft, target)
+    for b, (path, bonus) in enumerate([([0, 1, 3, 5], 40), ([0, 5, 6], 42)]):
+        r = res[b]
+        assert r["path"] == path and r["accept_len"] == len(path) and r["bonus"] == bonus
+        assert r["L_new"] == L + len(path)
+        seqK = np.concatenate([rawK[b, :L], treeK[b, path]])
+        seqV = np.concatenate([rawV[b, :L], treeV[b, path]])
+        assert np.array_equal(r["raw_rows"][0], treeK[b, path])
+        assert np.array_equal(r["raw_rows"][1], treeV[b, path])
+        want = {(m, (e + 1) // m - 1) for m in ms for e in range(L, L + len(path)) if (e + 1) % m == 0}
+        assert set(r["entries"]) == want
+        for (m, j), (ck, cv) in r["entries"].items():
+            CK, CV = compress_prefix(seqK, seqV, L + len(path), m, g[m], "f64")
+            assert np.array_equal(ck, CK[j]) and np.array_equal(cv, CV[j])
+
