@@ -108,7 +108,8 @@ def _refresh():
     return [lambda st=st, L=L, n=n: p_refresh.test_refresh_equals_compress_from_scratch(st, L, n)
             for st in ("bf16", "f64")
             for L, n in [(250, 8), (253, 3), (255, 1), (127, 4), (120, 8)]] + [
-        p_refresh.test_capacity_is_enforced, p_refresh.test_tiny_round_golden]
+        p_refresh.test_capacity_is_enforced, p_refresh.test_commit_fills_every_capacity_exactly,
+        p_refresh.test_tiny_round_golden]
 
 
 def _round():
@@ -173,6 +174,16 @@ MUTANTS = [
     ("scratch block one position early", V.scratch_entries,
      "for t in range(end + 1 - m, end + 1)])\n            Vb",
      "for t in range(end - m, end)])\n            Vb", _verify_all),
+    ("root read from the raw rows", V.sequence_row, "if pos < L:", "if pos <= L:", _verify_all),
+    ("path not reversed", V.path_to_root, "return path[::-1]", "return path", _verify_all),
+    ("partial block compressed", C.compress_prefix, "0, L // m, m, g, store", "0, (L + m - 1) // m, m, g, store",
+     _compress),
+    ("bf16 rounding bit off by one", S._round_f64_to_bf16, "keep_lsb = (bits >> np.uint64(45))",
+     "keep_lsb = (bits >> np.uint64(44))", _storage),
+    ("capacity refused at an exact fit", R.refresh_commit_request, "if L + n > rawK.shape[0]:",
+     "if L + n >= rawK.shape[0]:", _refresh),
+    ("compressed capacity refused at an exact fit", R.refresh_commit_request,
+     "if j >= CK.shape[0]:", "if j >= CK.shape[0] - 1:", _refresh),
     # acceptance ([TSD-V4] §4.1)
     ("highest-index matching child", A.accept_walk, "                nxt = c\n                break",
      "                nxt = c", _accept),

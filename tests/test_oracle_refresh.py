@@ -59,6 +59,28 @@ def test_capacity_is_enforced():
                                {4: np.zeros(d)}, raw, raw.copy(), comp)
 
 
+def test_commit_fills_every_capacity_exactly():
+    # raw rows and compressed entries end exactly at their capacities: the last committed token
+    # closes the last block that fits, and the commit succeeds
+    rng = np.random.default_rng(5)
+    d, D, m, L = 8, 4, 4, 8
+    raw = np.zeros((L + D, d))
+    rawV = np.zeros((L + D, d))
+    raw[:L] = rng.standard_normal((L, d))
+    rawV[:L] = rng.standard_normal((L, d))
+    treeK = rng.standard_normal((D, d))
+    treeV = rng.standard_normal((D, d))
+    g = {m: rng.standard_normal(d)}
+    ck, cv = np.zeros(((L + D) // m, d)), np.zeros(((L + D) // m, d))
+    ck[:L // m], cv[:L // m] = compress_prefix(raw, rawV, L, m, g[m], "f64")
+    comp = {m: (ck, cv)}
+    L_new, _ = refresh_commit_request((m,), "f64", L, [0, 1, 2, 3], D, treeK, treeV, g, raw, rawV,
+                                      comp)
+    assert L_new == L + D == raw.shape[0]
+    CK, CV = compress_prefix(raw, rawV, L_new, m, g[m], "f64")
+    assert np.array_equal(ck, CK) and np.array_equal(cv, CV)
+
+
 def test_tiny_round_golden():
     from tree_speculative_verify_gb300 import workloads
     with open(GOLDEN) as f:
