@@ -156,7 +156,15 @@ MUTANTS = [
      "pos = [L + depth[v] + 1 for v in range(D)]", lambda: _plan() + _verify_a()),
     ("remainder tail rounds up", P.build_plan, "m_min * (pos[v] // m_min)",
      "m_min * ((pos[v] + 1) // m_min)", lambda: _plan() + _verify_a()),
+    ("window not clamped at 0", P.build_plan, "raw_lo = [max(0, pos[v] - W) for v in range(D)]",
+     "raw_lo = [pos[v] - W for v in range(D)]", lambda: _plan() + _verify_a()),
+    ("scratch visibility tests the viewer", P.build_plan, "(anc[v] >> u) & 1 and completes[m][u]",
+     "(anc[v] >> u) & 1 and completes[m][v]", lambda: _plan() + _verify_a()),
     # verify ([TSD-V4] §3.1, §3.2, §4.2)
+    ("scratch visibility transposed", V.visible_set, "if (plan.scr_vis[m][v] >> u) & 1:",
+     "if (plan.scr_vis[m][u] >> v) & 1:", _verify_all),
+    ("scratch block ends one early", V.scratch_entries, "end = plan.pos[u]", "end = plan.pos[u] - 1",
+     _verify_all),
     ("logit scale 1/d", V.attend, "/ math.sqrt(d)", "/ d", _verify_all),
     ("LSE in log2", V.attend, "LSE = (M + np.log(Z))[:, 0]", "LSE = (M + np.log2(Z))[:, 0]",
      _verify_all),
@@ -189,6 +197,8 @@ MUTANTS = [
      "                nxt = c", _accept),
     ("draft compared with the child's own target", A.accept_walk,
      "int(draft[c]) == int(target[cur])", "int(draft[c]) == int(target[c])", _accept),
+    ("node 1 never considered", A.accept_walk, "for c in range(1, D):", "for c in range(2, D):",
+     _accept),
     ("bonus from the draft", A.accept_walk, "return len(path), path, int(target[cur])",
      "return len(path), path, int(draft[cur])", _accept),
     # refresh ([TSD-V4] §4.2)
@@ -210,6 +220,7 @@ MUTANTS = [
     # indexer (the sparse C4 path)
     ("ties to the higher index", I.topk_ascending, "key=lambda j: (-float(scores[j]), j)",
      "key=lambda j: (-float(scores[j]), -j)", _indexer),
+    ("one entry short", I.topk_ascending, "order[:k]", "order[:k - 1]", _indexer),
     ("list not ascending", I.topk_ascending, "return np.sort(np.asarray(order[:k], dtype=np.int32))",
      "return np.asarray(order[:k], dtype=np.int32)", _indexer),
     ("scores summed in fp64", I.index_scores, "s = (s + prod).astype(np.float32)",
@@ -219,6 +230,8 @@ MUTANTS = [
     # storage rounding
     ("bf16 ties rounded up", S._round_f64_to_bf16, "(bits + half_minus_one + keep_lsb)",
      "(bits + half_minus_one + np.uint64(1))", _storage),
+    ("f64 storage rounded to f32", S.round_to_storage, "    if store == \"f64\":\n        return x.copy()",
+     "    if store == \"f64\":\n        return x.astype(np.float32).astype(np.float64)", _storage),
     ("f32 storage not rounded", S.round_to_storage,
      "return x.astype(np.float32).astype(np.float64)", "return x.copy()", _storage),
 ]
