@@ -37,6 +37,24 @@ def test_header_declares_the_entry_points():
     assert set(decls) == set(_lib.EXPORTS)
 
 
+def test_header_compiles_as_c_and_cxx(tmp_path):
+    # the boundary is plain C: the header alone compiles as C11 and as C++17, warnings as errors
+    import shutil
+    import subprocess
+    src = tmp_path / "use.c"
+    src.write_text('#include "treeverify.h"\n'
+                   'int probe(tv_shape* s) { return (int)tv_workspace_size(s) + s->B; }\n')
+    for cc, std in (("gcc", "-std=c11"), ("g++", "-std=c++17")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not installed")
+        args = [cc, std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                "-I", os.path.dirname(HEADER)]
+        if cc == "g++":
+            args += ["-x", "c++"]
+        r = subprocess.run(args + [str(src)], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in _declarations():
         assert hasattr(lib, name), name
