@@ -289,6 +289,19 @@ int tv_indexer_topk(const tv_shape* shape, int d_idx, const void* q_idx, const v
                     const int32_t* L, int32_t* sel, void* workspace, size_t ws_bytes,
                     int32_t* status, tv_stream_t stream);
 
+/*
+ * Testing aid for the failure path of the tensor-core attention (the report has no counterpart).
+ * Sets, for every later tv_tree_verify_attn launch of the tcgen05 kernel in this process:
+ *   timeout_ns     the bound of every device-side wait (default 2000000000 = 2 s; > 0);
+ *   withhold_tile  one KV tile index (within each work item's tile range) whose K copies the
+ *                  producers never issue, or -1 for none (the default).
+ * With a tile withheld, the MMA issuer's wait for that tile runs out after timeout_ns; the kernel
+ * then records TV_ERR_TIMEOUT in the status word, stops every CTA of the affected clusters,
+ * drains the copies and MMAs it did issue and returns, leaving the context usable.  Restore
+ * (2000000000, -1) afterwards.  Host errors: TV_ERR_ARG (timeout_ns <= 0 or withhold_tile < -1).
+ */
+int tv_debug_attn_timeout(int64_t timeout_ns, int32_t withhold_tile);
+
 #ifdef __cplusplus
 }
 #endif

@@ -108,3 +108,41 @@ def test_host_validation_rejects_null_before_launch():
                                  rb.vis128, rb.scrK4, rb.scrV4, rb.scrK128, rb.scrV128, 0.04, rb.O,
                                  rb.lse, small_ws, rb.status)
     assert e.value.code == -7
+
+
+def test_attention_wait_that_runs_out_reports_timeout_and_context_stays_usable():
+    """A bounded device-side wait runs out on purpose: with tv_debug_attn_timeout the tensor-core
+    attention's producers never issue the K copies of KV tile 2, so the MMA issuer's wait for that
+    tile expires after 200 us.  The kernel records TV_ERR_TIMEOUT, stops both CTAs of the pair,
+    drains the copies and MMAs it did issue and returns; nothing traps or hangs.  The next call on
+    the same context matches the oracle."""
+    from helpers import upload_prefix
+    wl = _wl(B=2, L=(700, 900))       # 5 KV tiles per request: C4 x2, C128, raw tail, extra
+    comp = oracle_prefix(wl)
+    res = run_oracle(wl, comp, with_refresh=False)
+    shape, st, rb = _setup(wl)
+    assert _lib.tv_attn_kernel_for(shape) == _lib.TV_ATTN_TCGEN05
+    upload_prefix(wl, st, comp)
+    engine.plan(shape, st, rb)
+    engine.branch_compress(shape, st, rb)
+    torch.cuda.synchronize()
+    assert int(rb.status.item()) == 0
+    _lib.tv_debug_attn_timeout(200_000, 2)
+    try:
+        engine.attention(shape, st, rb)
+        torch.cuda.synchronize()
+    finally:
+        _lib.tv_debug_attn_timeout(2_000_000_000, -1)
+    assert int(rb.status.item()) == -8
+    # the context is still usable and the next call is exact again
+    rb.status.zero_()
+    rb.O.fill_(float("nan"))
+    engine.attention(shape, st, rb)
+    torch.cuda.synchronize()
+    assert int(rb.status.item()) == 0
+    O = rb.O.float().cpu().numpy()
+    lse = rb.lse.cpu().numpy()
+    for b in range(wl.B):
+        err = np.abs(O[b] - res[b]["O"])
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3
+        assert np.abs(lse[b] - res[b]["LSE"]).max() <= 1e-2

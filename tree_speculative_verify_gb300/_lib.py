@@ -31,7 +31,7 @@ EXPORTS = (
     "tv_attn_kernel_for",
     "tv_build_ancestor_mask", "tv_prefill_compress", "tv_branch_compress",
     "tv_tree_verify_attn", "tv_accept_walk", "tv_refresh_commit", "tv_tree_verify_attn_noalloc",
-    "tv_indexer_workspace_size", "tv_indexer_topk",
+    "tv_indexer_workspace_size", "tv_indexer_topk", "tv_debug_attn_timeout",
 )
 
 
@@ -76,6 +76,7 @@ _SIGS = {
     "tv_indexer_workspace_size": ([_SHAPE], ctypes.c_size_t),
     "tv_indexer_topk": ([_SHAPE, ctypes.c_int] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
                         ctypes.c_int),
+    "tv_debug_attn_timeout": ([ctypes.c_int64, ctypes.c_int32], ctypes.c_int),
 }
 
 
@@ -221,3 +222,8 @@ def tv_indexer_topk(shape, d_idx, q_idx, k_idx, L, sel, workspace, status, strea
                                 _p(L), _p(sel), _p(workspace), ctypes.c_size_t(ws_bytes),
                                 _p(status), _stream(stream))
     _check("tv_indexer_topk", rc)
+
+
+def tv_debug_attn_timeout(timeout_ns, withhold_tile):
+    """Testing aid: the wait bound and a withheld KV tile of later tensor-core attention calls."""
+    _check("tv_debug_attn_timeout", load().tv_debug_attn_timeout(int(timeout_ns), int(withhold_tile)))

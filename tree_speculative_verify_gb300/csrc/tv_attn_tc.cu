@@ -7,14 +7,22 @@
 // heads sharing one K/V head, all D*H query rows of a request read the same compressed prefix, so
 // the prefix part is a dense (D*H) x entries x 512 contraction -- tensor-core work.
 //
-// Work item: a CTA pair (a cluster of 2) for request b, two consecutive 128-row tiles of the
-// request's D*H query rows (node-major), one half of the value dimension (256 of 512 columns of
-// O) and one chunk of the request's KV tiles.  The pair runs cta_group::2 MMAs (M = 256): the
-// leader issues them, each CTA's tensor core works on its own 128 rows, and every K / V tile is
-// split between the two CTAs' shared memory, so each SM ingests half of it.  (The rate at which
-// TMA fills one SM's shared memory, not the tensor cores, bounds a one-CTA design here.)  The two
-// value halves of a row tile compute the same S = Q K^T: a 128-row, 512-column fp32 O would fill
-// all 512 TMEM columns and leave none for S.
+// Work item: a cluster of four CTAs for request b, two consecutive 128-row tiles of the request's
+// D*H query rows (node-major) and one chunk of the request's KV tiles.  The cluster is two CTA
+// pairs that split the work of every KV tile by stage rather than by data:
+//   pair S (ranks 0-1)   S_t = Q K_t^T with cta_group::2 MMAs (M = 256: each CTA's tensor core on
+//                        its own 128 rows; N = tile entries; K = 512, A = Q from TMEM, B = K from
+//                        shared memory, split between the two CTAs), then the online softmax; each
+//                        CTA sends its rows' bf16 P_t to the CTA of the other pair that holds the
+//                        same rows, into that CTA's shared memory (st.async)
+//   pair O (ranks 2-3)   O += P_t V_t with cta_group::2 MMAs (A = P from shared memory, B = V,
+//                        N = 2 x 256 value columns), O for all 512 columns in TMEM
+// A 128-row fp32 O of all 512 columns fills the 512 TMEM columns of a CTA, so S and O cannot share
+// one; Q (512 dims as packed bf16 = 256 columns) and two S buffers fill pair S's TMEM instead.
+// Every S element is computed once, both pairs issue the same number of equally sized MMAs per
+// tile, and pair S keeps no Q in shared memory, which leaves it a deep ring of K slots.  The
+// running row maximum lives in pair S; when it grows (lazily, by more than 2^8) pair S sends the
+// rescale factor with P and pair O rescales its O rows before accumulating P_t.
 //
 // KV tiles (<= 128 entries each), in order: persistent C4 entries, persistent C128 entries, the raw
 // tail (positions t0 .. L-1), and one "extra" tile of 32 entries: the tree tokens (0..7), the C4
@@ -23,28 +31,25 @@
 // mask, scratch visibility) inside the softmax warps.
 //
 // Warp roles (352 threads per CTA):
-//   warp 0      TMA producer: Q once (8 boxes of 128 x 64, completing on the leader's barrier like
-//               every other copy of the pair); then, through a 3-slot ring of 32 KB,
-//               this CTA's share of every tile: for S, two slots of four 64-dim slices of N/2
-//               entries; for PV, one slot of the tile's entries x 128 value columns
-//   warp 1      both CTAs: allocate / free 512 TMEM columns (cta_group::2).  Leader lane 0 issues
-//               S_t = Q K_t^T  (M=256, N=entries rounded to 16, K=512; A and B K-major)
-//               O  += P_t V_t   (M=256, N=256, K=entries; A = P in TMEM, B = V MN-major)
-//               and releases ring slots, S buffers and O in both CTAs with multicast commits.
-//               Both CTAs' TMA loads complete on the leader's ring barriers (cta_group::2 TMA).
-//   warps 2..9  softmax, two threads per query row (one per half of a tile's columns): read S_t
-//               from TMEM, mask, online softmax with a lazily updated row maximum, write P_t back
-//               into the S columns as packed bf16, rescale O in TMEM when the maximum grows by
-//               more than 2^8, and finally write O.
-//   warp 10     lane 0: once every softmax warp of the CTA has stored P_t, signals the leader's
-//               p_full (leader: local arrive with expect_tx; follower: a 4-byte st.async).
-// TMEM columns: S/P double buffer at [0,128) and [128,256), O at [256,512).
-// Every mbarrier wait is bounded; on timeout the CTA records TV_ERR_TIMEOUT, stops issuing work,
-// drains its own copies and MMAs (bounded) and frees its TMEM.
+//   warp 0      TMA producer: pair S, this CTA's half of every tile's K entries x 512 dims (two
+//               32 KB slots of a 6-slot ring); pair O, the tile's entries x this CTA's 256 value
+//               columns (two 32 KB slots of a 4-slot ring).  All copies of a pair complete on its
+//               leader's barriers (cta_group::2 TMA).
+//   warp 1      both CTAs: allocate / free 512 TMEM columns (cta_group::2); the leader's lane 0
+//               issues the pair's MMAs and releases ring slots and buffers with multicast commits
+//   warps 2..9  pair S: Q rows into TMEM, then per tile the softmax, two threads per query row
+//               (one per half of the tile's columns) sharing one running maximum; pair O: per
+//               tile the (rare) O rescale, and at the end O / l out through TMA stores
+//   warp 10     lane 0: forwards this CTA's per-tile readiness to its pair leader (leader: local
+//               arrive with expect_tx; follower: a 4-byte st.async)
+// TMEM columns: pair S: S buffers at [0,128) and [128,256), Q at [256,512); pair O: O at [0,512).
+// Every wait is bounded; on timeout the CTA records TV_ERR_TIMEOUT, sets the abort flag of all
+// four CTAs, stops issuing work, drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "tv_attn_tc.cuh"
@@ -55,26 +60,28 @@ namespace tc {
 
 using namespace sm100;
 
-constexpr int kSmxWarps = 8;           // softmax warps: 4 (a thread per row) or 8 (two per row)
-constexpr int kSigWarp = 2 + kSmxWarps;          // forwards "P ready" to the leader
-constexpr int kThreads = 64 + 32 * kSmxWarps + 32;   // producer, MMA issuer, softmax, signal
-// Ring of 32 KB slots: the rate at which one SM's TMA copies complete is set mostly by the
-// number of mbarrier transactions (about 0.3 us each, nearly independent of their size up to
-// 64 KB), so a tile's K share (64 KB) takes two slots and its V share (32 KB) one.
-constexpr int kSlots = 3;
+constexpr int kClusterCtas = 4;
+constexpr int kSmxWarps = 8;                     // softmax / rescale warps, two threads per row
+constexpr int kSigWarp = 2 + kSmxWarps;          // forwards per-tile readiness to the pair leader
+constexpr int kThreads = 64 + 32 * kSmxWarps + 32;   // producer, MMA issuer, role warps, signal
 constexpr int kSlotBytes = 32768;
-constexpr int kKSlices = 4;        // 64-dim K slices (64 entries x 128 B, 8 KB) per slot
-constexpr int kVBlock = 16384;     // V slot: two 64-column blocks of 128 entries
-constexpr int kQBytes = 8 * 16384;
-constexpr int kDp = 8;                 // rows per section of the extra tile (D <= 8)
-constexpr int kExtraEntries = 32;      // tree | C4 scratch | C128 scratch | zeros
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr int kSSlots = 4;      // pair S: K ring (a tile's K share is two slots of 4 x 64 dims)
+constexpr int kOSlots = 4;      // pair O: V ring (a tile's V share is two slots of 128 columns)
+constexpr int kKSlices = 4;     // 64-dim K slices (64 entries x 128 B, 8 KB) per slot
+constexpr int kVBlock = 16384;  // V slot: two 64-column blocks of 128 entries
+constexpr int kPBytes = 32768;  // P of one tile for one CTA's rows: 128 rows x 128 entries bf16
+constexpr int kPMsg = kPBytes + 128 * 4;   // P and the rows' rescale factors, sent as one copy
+constexpr int kPBuf = 33 * 1024;           // a P buffer (1 KB aligned)
+constexpr int kDp = 8;          // rows per section of the extra tile (D <= 8)
+constexpr int kExtraEntries = 32;   // tree | C4 scratch | C128 scratch | zeros
+constexpr uint32_t kTmemQ = 256;     // pair S: Q columns
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // default bound of every wait
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P values stay below 2^8
 
 enum TileKind { kC4 = 0, kC128 = 1, kRaw = 2, kExtra = 3 };
 
 struct Params {
-  CUtensorMap mQ;
+  CUtensorMap mQ, mO;   // [B][DH][512], box 64 x 128 x 1: Q rows in, O rows out
   CUtensorMap mC4K, mC4V, mC128K, mC128V, mRawK, mRawV;
   CUtensorMap mTreeK, mTreeV, mS4K, mS4V, mS128K, mS128V;
   int B, D, H, DH, W, tail_mode, comp_mask, n_pairs, n_chunks;
@@ -95,6 +102,8 @@ struct Params {
   Paging pg;       // paged pools: C4 tiles are read through the page table; the C128 entries and
                    // the raw tail are first gathered into the workspace (contiguous per request)
   int tail_rows;   // rows per request of the gathered raw tail (paged pools only)
+  uint64_t timeout_ns;   // bound of every wait (kTimeoutNs unless a test shortens it)
+  int withhold_tile;     // test aid: the producers never issue this tile's K copies (-1: none)
 };
 
 struct Layout {
@@ -244,28 +253,106 @@ __global__ void gather_paged_kernel(Paging pg, int comp_mask, int W, int tail_mo
   }
 }
 
-struct __align__(1024) Smem {
-  uint8_t q[kQBytes];
-  uint8_t ring[kSlots][kSlotBytes];
-  uint64_t full[kSlots];       // (leader) both CTAs' shares of a fill have landed
-  uint64_t empty[kSlots];      // the pair's MMAs are done with the slot
-  uint64_t q_full;             // (leader) both CTAs' Q rows have landed
-  uint64_t s_full[2];
-  uint64_t p_full[2];          // (leader) P written by both CTAs' softmax warps: the leader's
-                               // arrive with expect_tx(4) + the follower's 4-byte st.async
-  uint32_t p_flag[2];          // (leader) landing word of the follower's st.async
-  uint64_t p_local[2];         // this CTA's softmax warps have written P (one arrive per warp)
-  uint64_t pv_done;
-  uint64_t o_full;
+// Shared memory.  The operand buffers differ between the two pairs; the barriers and small arrays
+// sit at the same offsets in every CTA, so a commit or an asynchronous store of one pair can
+// target the other pair's barriers by offset.
+struct Header {
+  uint64_t full[kSSlots];      // (pair leader) both CTAs' shares of a fill have landed
+  uint64_t empty[kSSlots];     // the pair's MMAs are done with the slot
+  uint64_t q_full;             // pair S (leader): both CTAs' Q rows are in TMEM
+  uint64_t q_local;            // pair S: this CTA's role warps have written their Q rows
+  uint64_t q_tma;              // pair S: this CTA's Q rows have landed in the ring (TMA)
+  uint64_t s_full[2];          // pair S: S_t is in TMEM
+  uint64_t s_read[2];          // pair S: this CTA's softmax warps have read S_t (one per warp)
+  uint64_t s_free[2];          // pair S (leader): both CTAs' softmax warps have read S_t
+  uint64_t p_staged[2];        // pair S: this CTA's softmax warps have staged P_t (one per warp)
+  uint64_t stage_free[2];      // pair S: the copy of the staged P_{t-2} has read its buffer
+  uint64_t p_free[2];          // pair S: pair O's MMAs are done with the P buffer of parity t
+  uint64_t p_in[2];            // pair O: the row partner's P_t and rescale factors have landed
+  uint64_t p_local[2];         // pair O: this CTA's role warps have applied tile t's rescale
+  uint64_t p_full[2];          // pair O (leader): both CTAs are ready for PV_t
+  uint64_t pv_done;            // pair O: PV_t complete
+  uint64_t o_full;             // pair O: every PV complete
+  uint64_t ml_full;            // pair O: the row partner's final (m, l) have landed
   uint64_t drain;
-  float xmax[2][2][128];       // [tile parity][column half][row] partial row maxima
-  int xok[2][2][4];            // [tile parity][column half][lane quadrant] the warp carries on
+  uint64_t stage_full;         // pair O: the role warps have staged their O rows
+  uint32_t flag[4];            // (leader) landing words of the follower's 4-byte signals
+  float xmax[2][2][128];       // pair S: [tile parity][column half][row] partial row maxima
+  float xsum[2][128];          // pair S: [column half][row] partial row sums
+  float ml[128][2];            // pair O: [row] final (m, l) sent by pair S
+  int xok[2][2][4];            // pair S: [tile parity][column half][lane quadrant] carries on
   uint32_t tmem;
   int abort;
 };
+// A P buffer holds 128 rows x 128 entries of bf16 P as two 64-entry panels (K-major, 128-byte
+// swizzle), followed by the 128 rows' fp32 rescale factors.
+struct __align__(1024) Smem {
+  // pair S: the K ring (kSSlots x 32 KB), then two P staging buffers; pair O: two P buffers, then
+  // the V ring (kOSlots x 32 KB)
+  uint8_t buf[kSSlots * kSlotBytes + 2 * kPBuf];
+  Header h;
+};
+static_assert(2 * kPBuf + kOSlots * kSlotBytes <= kSSlots * kSlotBytes + 2 * kPBuf,
+              "pair O buffers");
+static_assert(sizeof(Smem) <= 232448, "shared memory of one CTA exceeds the 227 KB limit");
+
+// 3-D tile load into this CTA's shared memory, completing this CTA's own mbarrier.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
+                                             uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(v), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+          cluster_addr),
+      "r"(a), "r"(b), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
+}
 
 __device__ __forceinline__ void fail(Smem& sm, int32_t* status) {
-  if (atomicExch(&sm.abort, 1) == 0) record_error(status, TV_ERR_TIMEOUT);
+  if (atomicExch(&sm.h.abort, 1) == 0) {
+    record_error(status, TV_ERR_TIMEOUT);
+    // the other three CTAs stop waiting on this one
+    const uint32_t me = cluster_rank();
+    for (uint32_t r = 0; r < kClusterCtas; ++r)
+      if (r != me) st_cluster_u32(mapa_cluster(smem_u32(&sm.h.abort), r), 1u);
+  }
+}
+
+// A per-tile signal from a CTA to its pair leader: the leader arrives on its own barrier with
+// expect_tx(4); the follower completes those 4 bytes with an asynchronous store into the leader's
+// shared memory, which lands much sooner than a cluster-scope release-arrive.
+__device__ __forceinline__ void signal_leader(Smem& sm, uint64_t* bar, uint32_t* flag, bool leader,
+                                              uint32_t leader_rank, uint32_t value) {
+  if (leader)
+    mbar_arrive_expect_tx(bar, 4);
+  else
+    st_async_b32(mapa_cluster(smem_u32(flag), leader_rank), value,
+                 mapa_cluster(smem_u32(bar), leader_rank));
 }
 
 // Row (in its tensor map) of entry `idx` of a C4 / C128 / raw tile of request b.  Contiguous
@@ -284,109 +371,130 @@ __device__ __forceinline__ int64_t tile_row(const Params& p, int kind, int b, in
   return (int64_t)b * p.raw_cap + idx;
 }
 
-// ---- producer (warp 0 of both CTAs) --------------------------------------------------------
+// A descriptor's start-address field is (address >> 4) in its low 14 bits; every operand here
+// lies below 256 KB of shared memory, so adding (offset >> 4) never carries out of the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_offset) {
+  return desc + (uint64_t)(byte_offset >> 4);
+}
+
+// ---- ring of slots shared by a pair (the leader's full barriers count both CTAs' shares) ------
+struct Ring {
+  uint8_t* base;
+  int n;         // slots
+  int slot;
+  uint32_t phase;
+  __device__ void advance() {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// ---- producer (warp 0, lane 0 does the copies) -------------------------------------------------
+// Pair S: this CTA's half of every tile's K entries (N/2 rows), all 512 dims, in two slots of four
+// 64-dim slices.  Pair O: every entry of the tile for this CTA's 256 value columns, in two slots
+// (one per 256-column group of O) of two 64-column blocks; rows past the tile's entry count
+// rounded up to 64 are not loaded.
 template <bool kPaged>
-__device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uint32_t rank,
+__device__ void producer(const Params& p, Smem& sm, int b, int rt, bool role_s, uint32_t sub,
                          const Layout& y, int tb, int te) {
   const int lane = threadIdx.x & 31;
-  int slot = 0;
-  uint32_t phase = 0;
-  bool issued[kSlots];
-  uint32_t issued_phase[kSlots];
+  const uint32_t leader = cluster_rank() & ~1u;
+  Ring r{role_s ? sm.buf : sm.buf + 2 * kPBuf, role_s ? kSSlots : kOSlots, 0, 0};
+  bool issued[kSSlots];
+  uint32_t issued_phase[kSSlots];
 #pragma unroll
-  for (int i = 0; i < kSlots; ++i) {
+  for (int i = 0; i < kSSlots; ++i) {
     issued[i] = false;
     issued_phase[i] = 0;
   }
-  if (lane == 0) {
-    // both CTAs' Q rows complete on the leader's q_full: the pair's MMAs read both
-    const uint32_t q_bar = mapa_cluster(smem_u32(&sm.q_full), 0);
-    if (rank == 0) mbar_arrive_expect_tx(&sm.q_full, 2 * kQBytes);
-    for (int s = 0; s < 8; ++s)
-      tma_load_3d_pair(sm.q + s * 16384, &p.mQ, 64 * s, 128 * rt, b, q_bar);
-  }
   auto acquire = [&]() -> bool {
-    if (!mbar_wait(&sm.empty[slot], phase ^ 1, &sm.abort, kTimeoutNs)) {
+    if (!mbar_wait(&sm.h.empty[r.slot], r.phase ^ 1, &sm.h.abort, p.timeout_ns)) {
       if (lane == 0) fail(sm, p.status);
       return false;
     }
     return true;
   };
-  auto advance = [&]() {
-    issued[slot] = true;
-    issued_phase[slot] = phase;
-    if (++slot == kSlots) {
-      slot = 0;
-      phase ^= 1;
-    }
+  auto leader_full = [&]() { return mapa_cluster(smem_u32(&sm.h.full[r.slot]), leader); };
+  auto expect = [&](uint32_t bytes) {
+    if (sub == 0) mbar_arrive_expect_tx(&sm.h.full[r.slot], 2 * bytes);
+  };
+  auto finish = [&](bool loads) {
+    issued[r.slot] = loads;
+    issued_phase[r.slot] = r.phase;
+    r.advance();
   };
   const int tree_row = b * p.D;
-  // both CTAs' shares of a fill complete on the leader's full[slot]; the leader expects both
-  auto leader_full = [&](int sl) { return mapa_cluster(smem_u32(&sm.full[sl]), 0); };
-  auto expect = [&](uint32_t bytes) {
-    if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
-  };
-  // S operand: this CTA holds entries [rank * nqk/2, (rank+1) * nqk/2) of the tile; one slot
-  // holds four 64-dim slices of those (up to 64) entries, 8 KB each.
-  // rows of a tile's boxes (this CTA's K half, the two V halves), computed one tile ahead so that
-  // with paged pools the page-table reads are in flight while the producer waits for slots
-  struct Rows {
-    int k, v0, v1;
-  };
-  auto rows_of = [&](int t) -> Rows {
-    Rows r{0, 0, 0};
-    if (t < tb || t >= te) return r;
+  bool ok = true;
+  // tile rows are computed one tile ahead, so that with paged pools the page-table reads are in
+  // flight while the producer waits for slots
+  auto row_of = [&](int t) -> int2 {
+    int2 rw = make_int2(0, 0);
+    if (t < tb || t >= te) return rw;
     const Tile x = tile_of(y, t);
-    if (x.kind == kExtra) return r;
-    r.k = (int)tile_row<kPaged>(p, x.kind, b, x.row0 + (int)rank * (x.nqk / 2), y.t0);
-    r.v0 = (int)tile_row<kPaged>(p, x.kind, b, x.row0, y.t0);
-    r.v1 = kPaged ? (int)tile_row<kPaged>(p, x.kind, b, x.row0 + 64, y.t0) : r.v0 + 64;
-    return r;
-  };
-  auto load_k = [&](const Tile& x, const Rows& rw) -> bool {
-    const int nh = x.nqk / 2;
-    for (int j = 0; j < 512 / (64 * kKSlices); ++j) {
-      if (!acquire()) return false;
-      if (lane == 0) {
-        uint8_t* dst = sm.ring[slot];
-        const uint32_t bar = leader_full(slot);
-        if (x.kind == kExtra) {
-          // leader: tree rows | C4 scratch rows; follower: C128 scratch rows | zero rows
-          expect(kKSlices * 2 * kDp * 128);
-          for (int ks = 0; ks < kKSlices; ++ks) {
-            const int xcol = 64 * (kKSlices * j + ks);
-            uint8_t* d = dst + ks * 8192;
-            if (rank == 0) {
-              tma_load_2d_pair(d, &p.mTreeK, xcol, tree_row, bar);
-              tma_load_2d_pair(d + kDp * 128, &p.mS4K, xcol, tree_row, bar);
-            } else {
-              tma_load_2d_pair(d, &p.mS128K, xcol, tree_row, bar);
-              tma_load_2d_pair(d + kDp * 128, &p.mTreeK, xcol, p.tree_rows, bar);
-            }
-          }
-        } else {
-          const CUtensorMap* m = x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
-          const int r = rw.k;
-          expect(kSlotBytes);
-          for (int ks = 0; ks < kKSlices; ++ks)
-            tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * j + ks), r, bar);
-        }
-      }
-      advance();
+    if (x.kind == kExtra) return rw;
+    if (role_s) {
+      rw.x = (int)tile_row<kPaged>(p, x.kind, b, x.row0 + (int)sub * (x.nqk / 2), y.t0);
+    } else {
+      rw.x = (int)tile_row<kPaged>(p, x.kind, b, x.row0, y.t0);
+      rw.y = kPaged ? (int)tile_row<kPaged>(p, x.kind, b, x.row0 + 64, y.t0) : rw.x + 64;
     }
-    return true;
+    return rw;
   };
-  // PV operand: every entry of the tile, this CTA's 128 of the pair's 256 value columns; one slot
-  // holds the tile's entries as two 64-column blocks of 128 rows (rows past the tile's entry
-  // count rounded up to 64 are not loaded).
-  auto load_v = [&](const Tile& x, const Rows& rw) -> bool {
-    const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
-    const int col0 = 256 * half + 128 * (int)rank;
-    {
-      if (!acquire()) return false;
-      if (lane == 0) {
-        uint8_t* dst = sm.ring[slot];
-        const uint32_t bar = leader_full(slot);
+  if (role_s) {
+    // Q of this CTA's 128 rows (8 slices of 64 dims, 16 KB each) arrives first, in the four ring
+    // slots, on this CTA's own barrier; the softmax warps move it into TMEM and the leader's MMA
+    // issuer then releases the slots.  These four fills complete the slots' first full phase
+    // without bytes.
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sm.h.q_tma, 8 * 16384);
+      for (int s = 0; s < 8; ++s)
+        tma_load_3d(sm.buf + s * 16384, &p.mQ, 64 * s, 128 * rt, b, &sm.h.q_tma);
+      if (sub == 0)
+        for (int i = 0; i < kSSlots; ++i) mbar_arrive(&sm.h.full[i]);
+    }
+    for (int i = 0; i < kSSlots; ++i) finish(false);
+  }
+  int2 cur = row_of(tb);
+  for (int t = tb; t < te && ok; ++t) {
+    const int2 next = row_of(t + 1);
+    const Tile x = tile_of(y, t);
+    for (int g = 0; g < 2 && ok; ++g) {
+      if (!acquire()) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = r.base + r.slot * kSlotBytes;
+      const uint32_t bar = leader_full();
+      bool loads = true;
+      if (role_s) {
+        loads = t != p.withhold_tile;   // test aid: the MMA issuer's wait for it runs out
+        if (lane == 0 && loads) {
+          if (x.kind == kExtra) {
+            // leader: tree rows | C4 scratch rows; follower: C128 scratch rows | zero rows
+            expect(kKSlices * 2 * kDp * 128);
+            for (int ks = 0; ks < kKSlices; ++ks) {
+              const int xcol = 64 * (kKSlices * g + ks);
+              uint8_t* d = dst + ks * 8192;
+              if (sub == 0) {
+                tma_load_2d_pair(d, &p.mTreeK, xcol, tree_row, bar);
+                tma_load_2d_pair(d + kDp * 128, &p.mS4K, xcol, tree_row, bar);
+              } else {
+                tma_load_2d_pair(d, &p.mS128K, xcol, tree_row, bar);
+                tma_load_2d_pair(d + kDp * 128, &p.mTreeK, xcol, p.tree_rows, bar);
+              }
+            }
+          } else {
+            const CUtensorMap* m =
+                x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
+            expect(kSlotBytes);
+            for (int ks = 0; ks < kKSlices; ++ks)
+              tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * g + ks), cur.x, bar);
+          }
+        }
+      } else if (lane == 0) {
+        const int col0 = 256 * g + 128 * (int)sub;
         if (x.kind == kExtra) {
           expect(2 * 4 * kDp * 128);
           for (int cb = 0; cb < 2; ++cb) {
@@ -399,164 +507,261 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, int half, uin
           }
         } else {
           const CUtensorMap* m = x.kind == kC4 ? &p.mC4V : x.kind == kC128 ? &p.mC128V : &p.mRawV;
+          const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
           expect(nvh * 2 * 8192);
-          for (int h = 0; h < nvh; ++h) {
-            const int r = h == 0 ? rw.v0 : rw.v1;
+          for (int h = 0; h < nvh; ++h)
             for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb, r, bar);
-          }
+              tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb,
+                               h == 0 ? cur.x : cur.y, bar);
         }
       }
-      advance();
+      finish(loads);
     }
-    return true;
-  };
-  bool ok = true;
-  Rows prev = rows_of(tb - 1), cur = rows_of(tb);
-  for (int t = tb; t < te && ok; ++t) {
-    const Rows next = rows_of(t + 1);
-    ok = load_k(tile_of(y, t), cur);
-    if (ok && t > tb) ok = load_v(tile_of(y, t - 1), prev);
-    prev = cur;
     cur = next;
   }
-  if (ok && te > tb) load_v(tile_of(y, te - 1), prev);
   // drain: no copy issued by the pair may still be in flight when the CTA exits (the leader's
-  // full and q_full barriers count both CTAs' shares; the closing cluster barrier covers the
-  // follower)
-  if (rank == 0) {
+  // full barriers count both CTAs' shares; the closing cluster barrier covers the follower)
+  if (sub == 0 && lane == 0) {
     volatile int never = 0;
-    for (int i = 0; i < kSlots; ++i)
-      if (issued[i]) mbar_wait(&sm.full[i], issued_phase[i], &never, kTimeoutNs / 4);
-    mbar_wait(&sm.q_full, 0, &never, kTimeoutNs / 4);
+    for (int i = 0; i < r.n; ++i)
+      if (issued[i]) mbar_wait(&sm.h.full[i], issued_phase[i], &never, p.timeout_ns / 4);
   }
 }
 
-// ---- leader lane 0 of warp 1: the pair's MMAs ---------------------------------------------------
-__device__ void mma_issuer(const Params& p, Smem& sm, const Layout& y, int tb, int te) {
-  const uint32_t tmem = sm.tmem;
-  const uint16_t pair = 0x3;
-  int slot = 0;
-  uint32_t phase = 0;
-  auto wait_slot = [&]() -> bool {
-    if (!mbar_wait(&sm.full[slot], phase, &sm.abort, kTimeoutNs)) {
-      fail(sm, p.status);
-      return false;
-    }
-    tc_fence_after();
-    return true;
-  };
-  auto release = [&]() {
-    mma2_commit_mc(&sm.empty[slot], pair);
-    if (++slot == kSlots) {
-      slot = 0;
-      phase ^= 1;
-    }
-  };
-  bool ok = mbar_wait(&sm.q_full, 0, &sm.abort, kTimeoutNs);
-  if (!ok) fail(sm, p.status);
+// ---- pair leaders, lane 0 of warp 1: the MMAs ------------------------------------------------
+// One thread issues every MMA of a pair, and a tcgen05.mma is accepted only about as fast as the
+// issuing thread reaches it: the instructions between two MMAs are not hidden behind the tensor
+// pipe.  So descriptors are built once, each MMA adds a compile-time offset, and the K-step loops
+// are unrolled without run-time branches.
+__device__ __forceinline__ bool wait_ring(const Params& p, Smem& sm, const Ring& r) {
+  if (!mbar_wait(&sm.h.full[r.slot], r.phase, &sm.h.abort, p.timeout_ns)) {
+    fail(sm, p.status);
+    return false;
+  }
   tc_fence_after();
-  const uint32_t q_base = smem_u32(sm.q);
-  const uint32_t idO = idesc_bf16_f32(256, 256, 0, 1);
-  auto pv = [&](int j) -> bool {
-    const Tile x = tile_of(y, tb + j);
-    if (!mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, &sm.abort, kTimeoutNs)) {
-      fail(sm, p.status);
-      return false;
-    }
+  return true;
+}
+
+// Pair S: S_t = Q K_t^T into S buffer t & 1 (M = 256, N = the tile's entries, K = 512: A = Q from
+// TMEM columns [256, 512), B = K from the ring).
+__device__ void mma_s(const Params& p, Smem& sm, const Layout& y, int tb, int te) {
+  const uint32_t tmem = sm.h.tmem;
+  const uint16_t pair = 0x3;
+  Ring r{sm.buf, kSSlots, 0, 0};
+  if (!mbar_wait(&sm.h.q_full, 0, &sm.h.abort, p.timeout_ns)) {
+    fail(sm, p.status);
+  } else {
     tc_fence_after();
-    const int nks = x.nqk / 16;
-    {
-      if (!wait_slot()) return false;
-      const uint32_t vbase = smem_u32(sm.ring[slot]);
-      for (int ks = 0; ks < nks; ++ks) {
-        const uint64_t bdesc = smem_desc_sw128(vbase + 2048 * ks, kVBlock, 1024);
-        mma2_ts(tmem + 256, tmem + 128 * (j & 1) + 8 * ks, bdesc, idO, (j > 0 || ks > 0) ? 1u : 0u);
-      }
-      release();
+    // Q is in both CTAs' TMEM: the ring slots that carried it go back to the producers
+    for (int i = 0; i < kSSlots; ++i) {
+      mma2_commit_mc(&sm.h.empty[r.slot], pair);
+      r.advance();
     }
-    mma2_commit_mc(&sm.pv_done, pair);
-    return true;
-  };
+    const uint64_t ring_desc = smem_desc_sw128(smem_u32(sm.buf), 16, 1024);
+    const int n = te - tb;
+    for (int i = 0; i < n; ++i) {
+      const Tile x = tile_of(y, tb + i);
+      const uint32_t idS = idesc_bf16_f32(256, x.nqk, 0, 0);
+      const uint32_t d_s = tmem + 128 * (i & 1);
+      // both CTAs' softmax warps have read S_{i-2} out of this buffer
+      if (i >= 2 && !mbar_wait(&sm.h.s_free[i & 1], ((i - 2) >> 1) & 1, &sm.h.abort,
+                               p.timeout_ns)) {
+        fail(sm, p.status);
+        break;
+      }
+      bool ok = true;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        if (!wait_ring(p, sm, r)) {
+          ok = false;
+          break;
+        }
+        const uint64_t kd = desc_add(ring_desc, (uint32_t)r.slot * kSlotBytes);
+#pragma unroll
+        for (int m = 0; m < 4 * kKSlices; ++m)
+          mma2_ts(d_s, tmem + kTmemQ + 8 * (4 * kKSlices * g + m),
+                  desc_add(kd, (m >> 2) * 8192 + 32 * (m & 3)), idS, (g | m) ? 1u : 0u);
+        mma2_commit_mc(&sm.h.empty[r.slot], pair);
+        r.advance();
+      }
+      if (!ok) break;
+      mma2_commit_mc(&sm.h.s_full[i & 1], pair);
+    }
+  }
+  // drain every MMA this thread issued before TMEM is released
+  mma2_commit_mc(&sm.h.drain, 0x1);
+  volatile int never = 0;
+  mbar_wait(&sm.h.drain, 0, &never, p.timeout_ns / 4);
+}
+
+// Pair O: O[:, 256g .. 256g+255] += P_t V_t[:, 256g .. 256g+255] for g = 0, 1 (M = 256, N = 256,
+// K = the tile's entries: A = P from the P buffer of parity t, B = V from the ring).
+__device__ void mma_o(const Params& p, Smem& sm, const Layout& y, int tb, int te) {
+  const uint32_t tmem = sm.h.tmem;
+  const uint16_t pair = 0xC, pair_s = 0x3;
+  Ring r{sm.buf + 2 * kPBuf, kOSlots, 0, 0};
+  const uint64_t p_desc = smem_desc_sw128(smem_u32(sm.buf), 16, 1024);
+  const uint64_t ring_desc = smem_desc_sw128(smem_u32(r.base), kVBlock, 1024);
+  const uint32_t idO = idesc_bf16_f32(256, 256, 0, 1);
   const int n = te - tb;
+  bool ok = true;
   for (int i = 0; i < n && ok; ++i) {
     const Tile x = tile_of(y, tb + i);
-    const uint32_t idS = idesc_bf16_f32(256, x.nqk, 0, 0);
-    const uint32_t d_s = tmem + 128 * (i & 1);
-    for (int j = 0; j < 512 / (64 * kKSlices) && ok; ++j) {
-      if (!wait_slot()) {
+    const int nks = x.nqk / 16;
+    if (!mbar_wait(&sm.h.p_full[i & 1], (i >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
+      fail(sm, p.status);
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // P of this tile: two 64-entry panels of 128 rows x 128 B (K-major, 128-byte swizzle)
+    const uint64_t pd = desc_add(p_desc, (uint32_t)(i & 1) * kPBuf);
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      if (!wait_ring(p, sm, r)) {
         ok = false;
         break;
       }
-      const uint32_t kbase = smem_u32(sm.ring[slot]);
-      for (int ks = 0; ks < kKSlices; ++ks)
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc_sw128(q_base + (kKSlices * j + ks) * 16384 + 32 * kk, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kbase + ks * 8192 + 32 * kk, 16, 1024);
-          mma2_ss(d_s, a, bd, idS, (j | ks | kk) ? 1u : 0u);
-        }
-      release();
+      const uint64_t vd = desc_add(ring_desc, (uint32_t)r.slot * kSlotBytes);
+      const uint32_t od = tmem + 256 * g;
+      if (nks == 8) {
+        mma2_ss(od, pd, vd, idO, i > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 1; ks < 8; ++ks)
+          mma2_ss(od, desc_add(pd, (ks >> 2) * 16384 + 32 * (ks & 3)), desc_add(vd, 2048 * ks),
+                  idO, 1u);
+      } else {
+        for (int ks = 0; ks < nks; ++ks)
+          mma2_ss(od, desc_add(pd, (ks >> 2) * 16384 + 32 * (ks & 3)), desc_add(vd, 2048 * ks),
+                  idO, (i > 0 || ks > 0) ? 1u : 0u);
+      }
+      mma2_commit_mc(&sm.h.empty[r.slot], pair);
+      r.advance();
     }
     if (!ok) break;
-    mma2_commit_mc(&sm.s_full[i & 1], pair);
-    if (i >= 1) ok = pv(i - 1);
+    mma2_commit_mc(&sm.h.pv_done, pair);
+    mma2_commit_mc(&sm.h.p_free[i & 1], pair_s);   // pair S may overwrite this P buffer
   }
-  if (ok && n > 0) ok = pv(n - 1);
-  if (ok) mma2_commit_mc(&sm.o_full, pair);
-  // drain every MMA this thread issued before TMEM is released
-  mma2_commit_mc(&sm.drain, 0x1);
+  if (ok) mma2_commit_mc(&sm.h.o_full, pair);
+  mma2_commit_mc(&sm.h.drain, (uint16_t)(1u << cluster_rank()));
   volatile int never = 0;
-  mbar_wait(&sm.drain, 0, &never, kTimeoutNs / 4);
+  mbar_wait(&sm.h.drain, 0, &never, p.timeout_ns / 4);
 }
 
-// ---- softmax / epilogue (softmax warps of both CTAs) ----------------------------------------
-// kSmxWarps warps; warp w (>= 2) serves TMEM lane quadrant w % 4 (rows 32*(w%4) .. +31).  With 8
-// warps, two threads share a row (column half ch = (w-2)/4 each) and exchange their partial row
-// maxima through shared memory once per tile; with 4 warps one thread owns the whole row.  Both
-// threads of a row apply the same running maximum; partial row sums are combined at the end.
-constexpr int kCh = kSmxWarps / 4;          // threads per row
-constexpr int kColsPerThread = 128 / kCh;   // S columns per thread and tile
-constexpr int kOColsPerThread = 256 / kCh;  // O columns per thread
+// ---- signal warps (lane 0) -----------------------------------------------------------------------
+// Pair S: Q in this CTA's TMEM -> q_full; S_t read by this CTA's softmax warps -> s_free.
+// Pair O: tile t's rescale applied and P_t landed in this CTA -> p_full.  A follower cannot signal
+// tile t + 2 before the leader's barrier of tile t completed (the pipelines make the later signal
+// depend on the earlier one), so two parities suffice.
+// Pair S also moves P: once this CTA's softmax warps have staged P_t (and pair O's MMAs are done
+// with the destination buffer, the PV of tile t-2), one bulk copy takes the staged buffer to the
+// row partner's P buffer of parity t and completes its p_in barrier; the copy of P_t having read
+// its staging buffer frees that buffer for P_{t+2}.
+__device__ void signal_s(const Params& p, Smem& sm, int n, uint32_t rank) {
+  const uint32_t leader = rank & ~1u;
+  const bool is_leader = (rank & 1u) == 0;
+  const uint32_t partner = rank + 2;
+  if (!mbar_wait(&sm.h.q_local, 0, &sm.h.abort, p.timeout_ns)) {
+    fail(sm, p.status);
+    return;
+  }
+  signal_leader(sm, &sm.h.q_full, &sm.h.flag[0], is_leader, leader, 1u);
+  const uint32_t dst0 = mapa_cluster(smem_u32(sm.buf), partner);
+  const uint32_t bar0 = mapa_cluster(smem_u32(&sm.h.p_in[0]), partner);
+  const uint32_t src0 = smem_u32(sm.buf + kSSlots * kSlotBytes);
+  for (int i = 0; i < n; ++i) {
+    const int sb = i & 1;
+    const uint32_t ph = (i >> 1) & 1;
+    if (!mbar_wait(&sm.h.s_read[sb], ph, &sm.h.abort, p.timeout_ns)) {
+      fail(sm, p.status);
+      return;
+    }
+    signal_leader(sm, &sm.h.s_free[sb], &sm.h.flag[1 + sb], is_leader, leader, (uint32_t)i);
+    if (!mbar_wait(&sm.h.p_staged[sb], ph, &sm.h.abort, p.timeout_ns) ||
+        (i >= 2 && !mbar_wait(&sm.h.p_free[sb], ((i - 2) >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
+      fail(sm, p.status);
+      return;
+    }
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst0 + (uint32_t)sb * kPBuf),
+        "r"(src0 + (uint32_t)sb * kPBuf), "r"((uint32_t)kPMsg), "r"(bar0 + (uint32_t)sb * 8)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    // the copy of P_{i-1} has read its staging buffer: P_{i+1} may be staged there
+    if (i >= 1) {
+      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      mbar_arrive(&sm.h.stage_free[sb ^ 1]);
+    }
+  }
+  // every copy has read its source before the CTA moves on
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
+__device__ void signal_o(const Params& p, Smem& sm, int n, uint32_t rank) {
+  const uint32_t leader = rank & ~1u;
+  const bool is_leader = (rank & 1u) == 0;
+  for (int i = 0; i < n; ++i) {
+    if (!mbar_wait(&sm.h.p_local[i & 1], (i >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
+      fail(sm, p.status);
+      return;
+    }
+    signal_leader(sm, &sm.h.p_full[i & 1], &sm.h.flag[1 + (i & 1)], is_leader, leader,
+                  (uint32_t)i);
+  }
+}
+
+// ---- pair S role warps: Q into TMEM, then the softmax ------------------------------------------
+// Warp w (2..9) serves TMEM lane quadrant w % 4 (rows 32*(w%4) .. +31) and column half
+// ch = (w-2)/4 of each tile.  The two threads of a row exchange their partial row maxima through
+// shared memory once per tile and apply the same running maximum.
 __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
 
-// ---- signal warp: P of tile i is in both CTAs' TMEM -> the leader's MMA issuer ----------------
-// Lane 0 waits until all softmax warps of this CTA have stored P_i (local barrier).  The leader
-// then arrives on its own p_full with expect_tx(4); the follower completes those 4 bytes with an
-// asynchronous 4-byte store into the leader's shared memory (st.async with complete_tx), which
-// lands much sooner than a cluster-scope release-arrive.  The follower cannot signal tile i + 2
-// before p_full(i) completed: its S(i+2) needs the leader's PV(i), issued after p_full(i).
-__device__ void p_signal(const Params& p, Smem& sm, int n, uint32_t rank) {
-  const uint32_t flag_leader[2] = {mapa_cluster(smem_u32(&sm.p_flag[0]), 0),
-                                   mapa_cluster(smem_u32(&sm.p_flag[1]), 0)};
-  const uint32_t bar_leader[2] = {mapa_cluster(smem_u32(&sm.p_full[0]), 0),
-                                  mapa_cluster(smem_u32(&sm.p_full[1]), 0)};
-  for (int i = 0; i < n; ++i) {
-    const int sb = i & 1;
-    if (!mbar_wait(&sm.p_local[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs)) {
-      fail(sm, p.status);
-      return;
-    }
-    if (rank == 0)
-      mbar_arrive_expect_tx(&sm.p_full[sb], 4);
-    else
-      st_async_signal(flag_leader[sb], (uint32_t)i, bar_leader[sb]);
-  }
-}
-
-__device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int half, int chunk,
-                                 const Layout& y, int tb, int te) {
+__device__ void softmax_s(const Params& p, Smem& sm, int b, int rt, uint32_t rank, const Layout& y,
+                          int tb, int te) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
-  const int ch = (warp - 2) >> 2;           // always 0 with 4 softmax warps
+  const int ch = (warp - 2) >> 2;
   const int row = 32 * quad + lane;
   const int grow = 128 * rt + row;
   const bool row_ok = grow < p.DH;
-  const uint32_t tmem = sm.tmem;
+  const uint32_t tmem = sm.h.tmem;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const float sl2 = p.scale_log2;
+  const int n = te - tb;
+
+  bool ok = true;
+  // Q dims 256ch .. 256ch+255 of this row into TMEM columns 256 + 128ch ..: column c holds dims
+  // 2c (low half) and 2c + 1, the A-operand layout of a kind::f16 MMA
+  {
+    // the producer's TMA put Q in the ring as 8 slices of 128 rows x 64 dims (128-byte swizzle:
+    // 16-byte chunk c of row r at chunk c ^ (r & 7)); this thread moves dims 256ch .. 256ch+255
+    // of its row (slices 4ch .. 4ch+3) into TMEM, 32 columns per slice
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.h.q_tma, 0, &sm.h.abort, p.timeout_ns))) {
+      fail(sm, p.status);
+      ok = false;   // the first tile's exchange lets the row's other warp leave too
+    }
+#pragma unroll 1
+    for (int sl = 0; sl < 4 && ok; ++sl) {
+      const uint8_t* line = sm.buf + (4 * ch + sl) * 16384 + (row >> 3) * 1024 + (row & 7) * 128;
+      uint32_t q[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(line + ((c ^ (row & 7)) << 4));
+        q[4 * c] = v.x;
+        q[4 * c + 1] = v.y;
+        q[4 * c + 2] = v.z;
+        q[4 * c + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_base + kTmemQ + 128 * ch + 32 * sl, q);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(&sm.h.q_local);
+  }
 
   // per-row visibility of the raw tail and of the extra tile
   int raw_lo = 0;
@@ -578,36 +783,43 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
     }
   }
 
+  // this row's line in the P staging buffers (panel ch, 128-byte swizzle: 16-byte chunk c of the
+  // row at chunk c ^ (row & 7)); the signal warp copies each staged buffer to the row partner (the
+  // CTA of pair O with the same rows)
+  const uint32_t partner = rank + 2;
+  uint8_t* const p_line = sm.buf + kSSlots * kSlotBytes + ch * 16384 + (row >> 3) * 1024 +
+                          (row & 7) * 128;
+
   float m_ref = -INFINITY, l_run = 0.f;
-  const int n = te - tb;
-  // The two warps of a row (column halves) meet at one named barrier per tile and one after the
-  // tiles.  A warp whose bounded wait ran out still takes each barrier until both warps leave the
-  // tile loop together (each tile's exchange carries both warps' flags), so neither waits on the
-  // other forever.
-  bool ok = true;
+  // The two warps of a row (column halves) meet at one named barrier per tile.  A warp whose
+  // bounded wait ran out still takes each barrier until both warps leave the tile loop together
+  // (each tile's exchange carries both warps' flags), so neither waits on the other forever.
   for (int i = 0; i < n; ++i) {
     const Tile x = tile_of(y, tb + i);
     const int sb = i & 1;
-    const int c0 = kColsPerThread * ch;     // first S column of this thread
-    // the wait result is made warp-uniform: tcgen05.ld below is warp-collective
+    const int c0 = 64 * ch;   // first S column of this thread
     if (ok && !__all_sync(0xffffffffu,
-                          mbar_wait(&sm.s_full[sb], (i >> 1) & 1, &sm.abort, kTimeoutNs))) {
+                          mbar_wait(&sm.h.s_full[sb], (i >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
       fail(sm, p.status);
       ok = false;
     }
-    float s[kColsPerThread];
+    float s[64];
     float raw_max = -INFINITY;
     if (ok) {
       tc_fence_after();
       {
         uint32_t* sr = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-        for (int c = 0; c < kColsPerThread / 32; ++c)
+        for (int c = 0; c < 2; ++c)
           if (c0 + 32 * c < x.nqk)
             tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32 * c,
                       *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
         tmem_wait_ld();
       }
+      // S_t is in registers: its buffer may take S_{t+2}
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.h.s_read[sb]);
       // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
       float mx[8];
 #pragma unroll
@@ -615,14 +827,14 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
       const bool full_tile = (x.kind == kC4 || x.kind == kC128) && x.valid >= 128;
       if (full_tile) {
 #pragma unroll
-        for (int j = 0; j < kColsPerThread; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+        for (int j = 0; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
       } else {
 #pragma unroll
-        for (int j = 0; j < kColsPerThread; ++j) {
+        for (int j = 0; j < 64; ++j) {
           const int col = c0 + j;
           bool vis = col < x.valid;
           if (x.kind == kRaw) vis = vis && (x.row0 + col >= raw_lo);
-          if (x.kind == kExtra) vis = col < 32 && ((extra_mask >> (col & 31)) & 1u);
+          if (x.kind == kExtra) vis = col < kExtraEntries && ((extra_mask >> (col & 31)) & 1u);
           s[j] = vis ? s[j] : -INFINITY;
           mx[j & 7] = fmaxf(mx[j & 7], s[j]);
         }
@@ -630,123 +842,183 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
       raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
     }
-    if (kCh == 2) {
-      sm.xmax[sb][ch][row] = raw_max;
-      if (lane == 0) sm.xok[sb][ch][quad] = ok ? 1 : 0;
-      pair_sync(quad);
-      raw_max = fmaxf(raw_max, sm.xmax[sb][ch ^ 1][row]);
-      if (ok && !sm.xok[sb][ch ^ 1][quad]) {   // the row's other warp gave up
-        fail(sm, p.status);
-        ok = false;
-      }
+    sm.h.xmax[sb][ch][row] = raw_max;
+    if (lane == 0) sm.h.xok[sb][ch][quad] = ok ? 1 : 0;
+    pair_sync(quad);
+    raw_max = fmaxf(raw_max, sm.h.xmax[sb][ch ^ 1][row]);
+    if (ok && !sm.h.xok[sb][ch ^ 1][quad]) {   // the row's other warp gave up
+      fail(sm, p.status);
+      ok = false;
     }
     if (!ok) break;
     const float mt = raw_max * sl2;
     const bool grow_max = mt > m_ref + kRescaleThreshold;
     const float m_new = grow_max ? mt : m_ref;
+    // exactly 1 unless the maximum grows past a finite reference: pair O rescales O by it
     const float alpha = (grow_max && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-    // rescale this thread's O columns in TMEM before P_i is accumulated onto them (rare)
-    const bool need_rescale = grow_max && m_ref != -INFINITY && i > 0;
-    if (__any_sync(0xffffffffu, need_rescale)) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.pv_done, (i - 1) & 1, &sm.abort, kTimeoutNs))) {
-        fail(sm, p.status);
-        ok = false;   // the tile loop ends at the next exchange, together with the other warp
-        continue;
-      }
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < kOColsPerThread / 8; ++c) {
-        uint32_t r[8];
-        const uint32_t col = tmem + lane_base + 256 + kOColsPerThread * ch + 8 * c;
-        tmem_ld8(col, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-        tmem_st8(col, r);
-      }
-      tmem_wait_st();
-    }
     const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
     float sum[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) sum[k] = 0.f;
+    uint32_t pk[32];
 #pragma unroll
-    for (int c = 0; c < kColsPerThread / 64; ++c) {
-      uint32_t pk[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p0 = ex2_approx(fmaf(s[64 * c + 2 * j], sl2, neg_m));
-        const float p1 = ex2_approx(fmaf(s[64 * c + 2 * j + 1], sl2, neg_m));
-        sum[j & 3] += p0 + p1;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        pk[j] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      // P column k holds entries 2k and 2k+1
-      if (c0 + 64 * c < x.nqk) tmem_st32(tmem + lane_base + 128 * sb + (c0 >> 1) + 32 * c, pk);
+    for (int j = 0; j < 32; ++j) {
+      const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg_m));
+      const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg_m));
+      sum[j & 3] += p0 + p1;
+      const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+      pk[j] = *reinterpret_cast<const uint32_t*>(&h);
     }
     const float tsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     l_run = l_run * alpha + tsum;
     m_ref = m_new;
-    tmem_wait_st();
-    tc_fence_before();
-    // each warp's rows of P are in TMEM; the signal warp forwards the CTA's readiness to the
-    // leader, so no softmax warp waits for the cross-CTA arrive
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.p_local[sb]);
-  }
-  if (ok && n > 0) {
-    if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, 0, &sm.abort, kTimeoutNs))) {
+    // the copy of P_{i-2} has read this staging buffer
+    if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sm.h.stage_free[sb], ((i - 2) >> 1) & 1,
+                                                     &sm.h.abort, p.timeout_ns))) {
       fail(sm, p.status);
       ok = false;
+      continue;   // the next tile's exchange lets the row's other warp leave too
     }
+    uint8_t* const line = p_line + sb * kPBuf;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    if (ch == 0)
+      reinterpret_cast<float*>(sm.buf + kSSlots * kSlotBytes + sb * kPBuf + kPBytes)[row] = alpha;
+    // the copy reads the staging buffer through the async proxy
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.h.p_staged[sb]);
   }
-  float l_tot = l_run;
-  if (kCh == 2) {
-    // combine the two partial row sums (both threads of a row share m_ref); once o_full has been
-    // observed every copy and MMA of this CTA's ring is done, so its first slot holds the exchange
-    float* xsum = reinterpret_cast<float*>(sm.ring[0]);
-    xsum[128 * ch + row] = l_run;
-    pair_sync(quad);
-    l_tot = l_run + xsum[128 * (ch ^ 1) + row];
-  }
+  // combine the two partial row sums (both threads of a row share m_ref); both warps of a row
+  // take this barrier, whatever happened in the tile loop
+  sm.h.xsum[ch][row] = l_run;
+  pair_sync(quad);
+  const float l_tot = l_run + sm.h.xsum[ch ^ 1][row];
   if (!ok) return;
-  tc_fence_after();
-  const int d = 512;
-  const int ocol = 256 * half + kOColsPerThread * ch;   // first O column of this thread
-  if (p.n_chunks == 1) {
-    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-    __nv_bfloat16* orow = p.O + ((int64_t)b * p.DH + grow) * d + ocol;
-    for (int c = 0; c < kOColsPerThread / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + 256 + kOColsPerThread * ch + 32 * c, r);
-      tmem_wait_ld();
-      if (row_ok) {
-        uint4 w[4];
-        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * k]) * inv,
-                                                         __uint_as_float(r[2 * k + 1]) * inv);
-          wp[k] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = w[k];
-      }
-    }
-    if (row_ok && half == 0 && ch == 0)
+  if (ch == 0) {
+    st_async_v2(mapa_cluster(smem_u32(&sm.h.ml[row][0]), partner), __float_as_uint(m_ref),
+                __float_as_uint(l_tot), mapa_cluster(smem_u32(&sm.h.ml_full), partner));
+    if (row_ok && p.n_chunks == 1)
       p.lse[(int64_t)b * p.DH + grow] =
           l_tot > 0.f ? (m_ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+// ---- pair O role warps: per-tile rescale, then the epilogue --------------------------------------
+// Warp w (2..9) serves lane quadrant w % 4 and O columns 256ch .. 256ch+255, ch = (w-2)/4.
+__device__ void rescale_epilogue_o(const Params& p, Smem& sm, int b, int rt, int chunk,
+                                   const Layout& y, int tb, int te) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int ch = (warp - 2) >> 2;
+  const int row = 32 * quad + lane;
+  const int grow = 128 * rt + row;
+  const bool row_ok = grow < p.DH;
+  const uint32_t tmem = sm.h.tmem;
+  const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+  const int n = te - tb;
+  const bool arms = row == 0 && ch == 0;   // the thread that arms the per-tile barriers
+  bool ok = true;
+  for (int i = 0; i < n; ++i) {
+    const int sb = i & 1;
+    if (arms) mbar_arrive_expect_tx(&sm.h.p_in[sb], kPMsg);
+    if (!__all_sync(0xffffffffu,
+                    mbar_wait(&sm.h.p_in[sb], (i >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
+      fail(sm, p.status);
+      ok = false;
+      break;
+    }
+    const float alpha = reinterpret_cast<const float*>(sm.buf + sb * kPBuf + kPBytes)[row];
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // O must hold every earlier PV before it is rescaled (tile 0 always sends 1)
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&sm.h.pv_done, (i - 1) & 1, &sm.h.abort, p.timeout_ns))) {
+        fail(sm, p.status);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 256 / 32; ++c) {
+        uint32_t r[32];
+        const uint32_t col = tmem + lane_base + 256 * ch + 32 * c;
+        tmem_ld32(col, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+        tmem_st32(col, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.h.p_local[sb]);
+  }
+  if (!ok) return;
+  float m = -INFINITY, l = 0.f;
+  if (n > 0) {
+    if (arms) mbar_arrive_expect_tx(&sm.h.ml_full, 128 * 8);
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.h.o_full, 0, &sm.h.abort, p.timeout_ns)) ||
+        !__all_sync(0xffffffffu, mbar_wait(&sm.h.ml_full, 0, &sm.h.abort, p.timeout_ns))) {
+      fail(sm, p.status);
+      return;
+    }
+    tc_fence_after();
+    m = sm.h.ml[row][0];
+    l = sm.h.ml[row][1];
+  }
+  const int d = 512;
+  if (p.n_chunks == 1) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // O leaves through shared memory and TMA stores: the V ring (idle once o_full has been
+    // observed) takes this CTA's 128 rows x 512 columns as eight 64-column boxes with the 128-byte
+    // swizzle; rows past D*H fall outside the map and are not stored
+    uint8_t* stage = sm.buf + 2 * kPBuf;
+    for (int c = 0; c < 256 / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_base + 256 * ch + 32 * c, r);
+      tmem_wait_ld();
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * k]) * inv,
+                                                       __uint_as_float(r[2 * k + 1]) * inv);
+        w[k] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const int col = 256 * ch + 32 * c;   // O column of w[0]
+      uint8_t* line = stage + (col >> 6) * 16384 + row * 128;
+      const int cc0 = (col & 63) >> 3;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(line + (((cc0 + q) ^ (row & 7)) << 4)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.h.stage_full);
+    // a bounded wait, not a CTA barrier: a role warp that gave up earlier never arrives
+    if (warp == 2 && lane == 0 && mbar_wait(&sm.h.stage_full, 0, &sm.h.abort, p.timeout_ns)) {
+      for (int k = 0; k < 8; ++k)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                reinterpret_cast<uint64_t>(&p.mO)),
+            "r"(64 * k), "r"(128 * rt), "r"(b), "r"(smem_u32(stage + k * 16384))
+            : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
   } else {
     float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + chunk) * (d + 4);
-    for (int c = 0; c < kOColsPerThread / 32; ++c) {
+    for (int c = 0; c < 256 / 32; ++c) {
       uint32_t r[32];
       if (n > 0) {
-        tmem_ld32(tmem + lane_base + 256 + kOColsPerThread * ch + 32 * c, r);
+        tmem_ld32(tmem + lane_base + 256 * ch + 32 * c, r);
         tmem_wait_ld();
       }
       if (row_ok) {
-        float4* dst = reinterpret_cast<float4*>(prow + ocol + 32 * c);
+        float4* dst = reinterpret_cast<float4*>(prow + 256 * ch + 32 * c);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           dst[k] = n > 0 ? make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
@@ -754,9 +1026,9 @@ __device__ void softmax_epilogue(const Params& p, Smem& sm, int b, int rt, int h
                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    if (row_ok && half == 0 && ch == 0) {
-      prow[d] = m_ref;
-      prow[d + 1] = l_tot;
+    if (row_ok && ch == 0) {
+      prow[d] = m;
+      prow[d + 1] = l;
     }
   }
 }
@@ -774,18 +1046,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid: clusters of 2 consecutive CTAs = the row tiles 2*pair and 2*pair+1
-  const uint32_t rank = blockIdx.x & 1;
-  int x = blockIdx.x >> 1;
-  const int half = x & 1;
-  x >>= 1;
+  // grid: clusters of 4 consecutive CTAs; rank = 2 * (0: pair S, 1: pair O) + (row tile & 1)
+  const uint32_t rank = blockIdx.x & 3;
+  const bool role_s = rank < 2;
+  const uint32_t sub = rank & 1;
+  int x = blockIdx.x >> 2;
   const int pair_idx = x % p.n_pairs;
   x /= p.n_pairs;
   const int chunk = x % p.n_chunks;
   const int b = p.order[x / p.n_chunks];
-  const int rt = 2 * pair_idx + (int)rank;
+  const int rt = 2 * pair_idx + (int)sub;
 
-  const Layout y = layout_of(p, b);   // identical in both CTAs of the pair
+  const Layout y = layout_of(p, b);   // identical in all four CTAs
   if (y.T == 0) {
     if (threadIdx.x == 0) record_error(p.status, TV_ERR_CAPACITY);
     return;
@@ -794,58 +1066,86 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   const int te = (int)((int64_t)y.T * (chunk + 1) / p.n_chunks);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], 1);
+    for (int i = 0; i < kSSlots; ++i) {
+      mbar_init(&sm.h.full[i], 1);
+      mbar_init(&sm.h.empty[i], 1);
     }
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.s_full[0], 1);
-    mbar_init(&sm.s_full[1], 1);
-    mbar_init(&sm.p_full[0], 1);
-    mbar_init(&sm.p_full[1], 1);
-    mbar_init(&sm.p_local[0], kSmxWarps);
-    mbar_init(&sm.p_local[1], kSmxWarps);
-    mbar_init(&sm.pv_done, 1);
-    mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.drain, 1);
-    sm.abort = 0;
+    mbar_init(&sm.h.q_full, 1);
+    mbar_init(&sm.h.q_local, kSmxWarps);
+    mbar_init(&sm.h.q_tma, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.h.s_full[i], 1);
+      mbar_init(&sm.h.s_read[i], kSmxWarps);
+      mbar_init(&sm.h.s_free[i], 1);
+      mbar_init(&sm.h.p_staged[i], kSmxWarps);
+      mbar_init(&sm.h.stage_free[i], 1);
+      mbar_init(&sm.h.p_free[i], 1);
+      mbar_init(&sm.h.p_in[i], 1);
+      mbar_init(&sm.h.p_local[i], kSmxWarps);
+      mbar_init(&sm.h.p_full[i], 1);
+    }
+    mbar_init(&sm.h.pv_done, 1);
+    mbar_init(&sm.h.o_full, 1);
+    mbar_init(&sm.h.ml_full, 1);
+    mbar_init(&sm.h.drain, 1);
+    mbar_init(&sm.h.stage_full, kSmxWarps);
+    sm.h.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.mQ);
-    prefetch_tmap(&p.mC4K);
-    prefetch_tmap(&p.mC4V);
+    prefetch_tmap(role_s ? &p.mC4K : &p.mC4V);
+    prefetch_tmap(role_s ? &p.mRawK : &p.mRawV);
   }
   if (warp == 1) {
-    tmem_alloc2(&sm.tmem, 512);
+    tmem_alloc2(&sm.h.tmem, 512);
     tmem_relinquish2();
   }
   tc_fence_before();
-  cluster_sync();   // both CTAs' barriers exist before any remote arrive or pair MMA
+  cluster_sync();   // every CTA's barriers exist before any remote arrive, store or pair MMA
   tc_fence_after();
 
   if (tb < te) {
     if (warp == 0) {
-      producer<kPaged>(p, sm, b, rt, half, rank, y, tb, te);
+      producer<kPaged>(p, sm, b, rt, role_s, sub, y, tb, te);
     } else if (warp == 1) {
-      if (lane == 0) {
-        if (rank == 0) mma_issuer(p, sm, y, tb, te);
+      if (lane == 0 && sub == 0) {
+        if (role_s)
+          mma_s(p, sm, y, tb, te);
+        else
+          mma_o(p, sm, y, tb, te);
       }
       __syncwarp();
     } else if (warp == kSigWarp) {
-      if (lane == 0) p_signal(p, sm, te - tb, rank);
+      if (lane == 0) {
+        if (role_s)
+          signal_s(p, sm, te - tb, rank);
+        else
+          signal_o(p, sm, te - tb, rank);
+      }
       __syncwarp();
+    } else if (role_s) {
+      softmax_s(p, sm, b, rt, rank, y, tb, te);
     } else {
-      softmax_epilogue(p, sm, b, rt, half, chunk, y, tb, te);
+      rescale_epilogue_o(p, sm, b, rt, chunk, y, tb, te);
     }
-  } else if (warp >= 2 && warp < kSigWarp) {
-    softmax_epilogue(p, sm, b, rt, half, chunk, y, tb, te);   // empty chunk: l = 0
+  } else if (warp >= 2 && warp < kSigWarp && !role_s) {
+    rescale_epilogue_o(p, sm, b, rt, chunk, y, tb, te);   // empty chunk: l = 0
   }
 
   tc_fence_before();
-  cluster_sync();   // the leader's MMAs are drained and no remote arrive is still in flight
+  cluster_sync();   // the leaders' MMAs are drained; every awaited remote store has landed
+  // after that barrier all four CTAs see the same abort flag (fail() sets the others' flags
+  // before its CTA arrives), so all take the same branch
+  if (*reinterpret_cast<volatile int*>(&sm.h.abort)) {
+    // a wait ran out in this cluster: give the copies and stores another CTA issued before it
+    // stopped (asynchronous ones included) time to land while all four CTAs are still resident
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 50000) {
+    }
+    cluster_sync();
+  }
   tc_fence_after();
-  if (warp == 1) tmem_dealloc2(sm.tmem, 512);
+  if (warp == 1) tmem_dealloc2(sm.h.tmem, 512);
 }
 
 }  // namespace tc
@@ -884,29 +1184,71 @@ bool make_map(CUtensorMap* m, const void* base, int rank, uint64_t rows, uint64_
 
 int n_pairs_of(const tv_shape* s) { return ((s->D * s->H + 127) / 128 + 1) / 2; }
 
-// Number of KV chunks per request.  Clusters of 2 CTAs run one per SM pair; a cluster costs about
-// (its tiles + 2) tile-times (the Q load and the epilogue).  With T the largest tile count the
-// capacities allow, pick the chunk count that minimises waves x (ceil(T / n) + 2); a larger count
-// must win by more than 10 % (splitting adds fp32 partials and a merge pass).
-int tc_chunks(const tv_shape* s) {
-  static int pair_slots = 0;
-  if (pair_slots == 0) {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 2)
-      sms = 152;
+// Per device, once: the kernels' shared-memory attribute and the number of 4-CTA clusters that
+// can be resident at a time (a plain host call that also stays out of any stream being captured).
+// Returns 0 on a CUDA error.
+int cluster_slots() {
+  static std::mutex mu;
+  static int slots[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
-    pair_slots = sms / 2;
+    return 0;
   }
+  std::lock_guard<std::mutex> lock(mu);
+  if (slots[dev] == 0) {
+    using namespace tv::tc;
+    const int smem = (int)sizeof(Smem);
+    if (cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<false>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+      }
+      n = sms / kClusterCtas > 0 ? sms / kClusterCtas : 1;
+    }
+    slots[dev] = n;
+  }
+  return slots[dev];
+}
+
+// Number of KV chunks per request.  Clusters of 4 CTAs run one per resident cluster slot; a
+// cluster costs about (its tiles + 4) tile-times (Q into TMEM, the first K and V fills, the O
+// epilogue).  With T the largest tile count the capacities allow, pick the chunk count that
+// minimises waves x (ceil(T / n) + 4); a larger count must win by more than 10 % (splitting adds
+// fp32 partials and a merge pass).
+int tc_chunks(const tv_shape* s) {
+  int slots = cluster_slots();
+  if (slots <= 0) slots = 36;
   int64_t max_tiles = 1 + (s->tail_mode == TV_TAIL_WINDOW ? (s->W + 127) / 128 : 1);
   if (s->comp_mask & TV_COMP_C4) max_tiles += ((s->n_sel > 0 ? s->n_sel : s->c4_cap) + 127) / 128;
   if (s->comp_mask & TV_COMP_C128) max_tiles += (s->c128_cap + 127) / 128;
-  const int64_t clusters1 = (int64_t)s->B * n_pairs_of(s) * 2;   // two value halves
+  const int64_t clusters1 = (int64_t)s->B * n_pairs_of(s);
   int best = 1;
   int64_t best_cost = -1;
   for (int n = 1; n <= 64 && n <= max_tiles; ++n) {
-    const int64_t waves = (clusters1 * n + pair_slots - 1) / pair_slots;
-    const int64_t cost = waves * ((max_tiles + n - 1) / n + 2);
+    const int64_t waves = (clusters1 * n + slots - 1) / slots;
+    const int64_t cost = waves * ((max_tiles + n - 1) / n + 4);
     if (best_cost < 0 || 10 * cost < 9 * best_cost) {
       best_cost = cost;
       best = n;
@@ -914,6 +1256,11 @@ int tc_chunks(const tv_shape* s) {
   }
   return best;
 }
+
+// Test aid (tv_debug_attn_timeout): the bound of every wait and one KV tile whose K copies the
+// producers withhold.
+std::atomic<int64_t> g_timeout_ns{(int64_t)tv::tc::kTimeoutNs};
+std::atomic<int32_t> g_withhold_tile{-1};
 
 }  // namespace
 
@@ -1023,7 +1370,7 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
     c128V = rawV;
   }
   const uint64_t trows = B * (uint64_t)s->D;
-  bool ok = make_map(&p.mQ, a.Q, 3, DH, B, 128);
+  bool ok = make_map(&p.mQ, a.Q, 3, DH, B, 128) && make_map(&p.mO, a.O, 3, DH, B, 128);
   ok = ok && make_map(&p.mC4K, c4K, 2, c4rows, 1, 64) && make_map(&p.mC4V, c4V, 2, c4rows, 1, 64);
   ok = ok && make_map(&p.mC128K, c128K, 2, c128rows, 1, 64) &&
        make_map(&p.mC128V, c128V, 2, c128rows, 1, 64);
@@ -1063,6 +1410,8 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.order = order;
   p.part = reinterpret_cast<float*>(ws + pre_partial_bytes(s));
   p.status = a.status;
+  p.timeout_ns = (uint64_t)g_timeout_ns.load();
+  p.withhold_tile = g_withhold_tile.load();
   if (gathered && s->B > 0) {
     const int64_t rows = (int64_t)s->B * s->n_sel;
     gather_sel_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
@@ -1086,25 +1435,10 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   // one CTA ranks all requests (B <= 12288 fits its default shared memory)
   order_kernel<<<1, 1024, (size_t)s->B * sizeof(int), stream>>>(p, order);
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;
+  if (cluster_slots() <= 0)
+    return tv_check_launch("tv_tree_verify_attn (tcgen05 kernel attributes)");
   const size_t smem = sizeof(Smem);
-  // once per device (a plain host call that also stays out of any stream being captured)
-  static std::mutex attr_mu;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-    return tv_check_launch("tv_tree_verify_attn (tcgen05 device query)");
-  {
-    std::lock_guard<std::mutex> lock(attr_mu);
-    if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem) != cudaSuccess ||
-          cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem) != cudaSuccess)
-        return tv_check_launch("tv_tree_verify_attn (tcgen05 shared-memory attribute)");
-      attr_set[dev] = true;
-    }
-  }
-  const unsigned grid = (unsigned)(s->B * p.n_chunks * p.n_pairs * 4);
+  const unsigned grid = (unsigned)(s->B * p.n_chunks * p.n_pairs * kClusterCtas);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -1112,7 +1446,7 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kClusterCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -1120,9 +1454,18 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   const cudaError_t le = paged ? cudaLaunchKernelEx(&cfg, attn_kernel<true>, p)
                                : cudaLaunchKernelEx(&cfg, attn_kernel<false>, p);
   if (le != cudaSuccess)
-    return tv_check_launch("tv_tree_verify_attn (tcgen05 pair launch)");
+    return tv_check_launch("tv_tree_verify_attn (tcgen05 cluster launch)");
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05)")) return rc;
   if (p.n_chunks > 1)
     return tv_launch_merge<__nv_bfloat16>(s->B, DH, 512, p.n_chunks, p.part, a.O, a.lse, stream);
+  return TV_OK;
+}
+
+extern "C" int tv_debug_attn_timeout(int64_t timeout_ns, int32_t withhold_tile) {
+  if (timeout_ns <= 0 || withhold_tile < -1)
+    return tv_set_error(TV_ERR_ARG, "tv_debug_attn_timeout: timeout_ns must be > 0 and "
+                                    "withhold_tile >= -1");
+  g_timeout_ns.store(timeout_ns);
+  g_withhold_tile.store(withhold_tile);
   return TV_OK;
 }
