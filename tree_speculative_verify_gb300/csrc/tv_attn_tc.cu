@@ -259,7 +259,7 @@ __global__ void gather_paged_kernel(Paging pg, int comp_mask, int W, int tail_mo
 struct Header {
   uint64_t full[kSSlots];      // (pair leader) both CTAs' shares of a fill have landed
   uint64_t empty[kSSlots];     // the pair's MMAs are done with the slot
-  uint64_t q_full;             // pair S (leader): both CTAs' Q rows are in TMEM
+  uint64_t q_full;             // pair S (leader): both CTAs' Q rows are in TMEM (one per item)
   uint64_t q_local;            // pair S: this CTA's role warps have written their Q rows
   uint64_t q_tma;              // pair S: this CTA's Q rows have landed in the ring (TMA)
   uint64_t s_full[2];          // pair S: S_t is in TMEM
@@ -272,28 +272,32 @@ struct Header {
   uint64_t p_local[2];         // pair O: this CTA's role warps have applied tile t's rescale
   uint64_t p_full[2];          // pair O (leader): both CTAs are ready for PV_t
   uint64_t pv_done;            // pair O: PV_t complete
-  uint64_t o_full;             // pair O: every PV complete
-  uint64_t ml_full;            // pair O: the row partner's final (m, l) have landed
+  uint64_t o_full;             // pair O: every PV of the item complete (one per item)
+  uint64_t o_free;             // pair O: the role warps have read the item's O out of TMEM
+  uint64_t stage_full;         // pair O: the role warps have staged the item's O rows
+  uint64_t v_free;             // pair O: the epilogue is done with the V ring
+  uint64_t ml_full[2];         // pair O: [item parity] the row partner's final (m, l) landed
   uint64_t drain;
-  uint64_t stage_full;         // pair O: the role warps have staged their O rows
   uint32_t flag[4];            // (leader) landing words of the follower's 4-byte signals
   float xmax[2][2][128];       // pair S: [tile parity][column half][row] partial row maxima
   float xsum[2][128];          // pair S: [column half][row] partial row sums
-  float ml[128][2];            // pair O: [row] final (m, l) sent by pair S
+  float ml[2][128][2];         // pair O: [item parity][row] final (m, l) sent by pair S
   int xok[2][2][4];            // pair S: [tile parity][column half][lane quadrant] carries on
+  int xok_end[2][4];           // pair S: [column half][lane quadrant] carries on after an item
   uint32_t tmem;
   int abort;
 };
 // A P buffer holds 128 rows x 128 entries of bf16 P as two 64-entry panels (K-major, 128-byte
 // swizzle), followed by the 128 rows' fp32 rescale factors.
 struct __align__(1024) Smem {
-  // pair S: the K ring (kSSlots x 32 KB), then two P staging buffers; pair O: two P buffers, then
-  // the V ring (kOSlots x 32 KB)
+  // pair S: the K ring (kSSlots x 32 KB, which also carries each item's Q), then two P staging
+  // buffers; pair O: two P buffers, then the V ring (kOSlots x 32 KB)
   uint8_t buf[kSSlots * kSlotBytes + 2 * kPBuf];
   Header h;
 };
 static_assert(2 * kPBuf + kOSlots * kSlotBytes <= kSSlots * kSlotBytes + 2 * kPBuf,
               "pair O buffers");
+static_assert(kSSlots * kSlotBytes == 8 * 16384, "an item's Q fills the K ring exactly");
 static_assert(sizeof(Smem) <= 232448, "shared memory of one CTA exceeds the 227 KB limit");
 
 // 3-D tile load into this CTA's shared memory, completing this CTA's own mbarrier.
@@ -322,14 +326,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t cluster_addr, uint32_t a, u
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
           cluster_addr),
       "r"(a), "r"(b), "r"(cluster_bar)
-      : "memory");
-}
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
       : "memory");
 }
 
@@ -377,6 +373,37 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_offset
   return desc + (uint64_t)(byte_offset >> 4);
 }
 
+// ---- work items ----------------------------------------------------------------------------------
+// The grid holds one cluster per resident cluster slot; cluster c walks the longest-first list of
+// work items (request, pair of row tiles, KV chunk) in a snake order: item c in round 0,
+// G + (G-1-c) in round 1, 2G + c in round 2, ... for G clusters, so that every cluster gets a mix
+// of long and short items.  Every role of every CTA of the cluster walks the same list.
+struct Item {
+  int b, rt, chunk, tb, te;
+  Layout y;
+};
+
+__device__ __forceinline__ bool item_at(const Params& p, int k, uint32_t sub, Item& it) {
+  const int G = (int)(gridDim.x / kClusterCtas), c = (int)(blockIdx.x / kClusterCtas);
+  const int pos = (k & 1) ? k * G + (G - 1 - c) : k * G + c;
+  if (pos >= p.B * p.n_chunks * p.n_pairs) return false;
+  int x = pos;
+  const int pair_idx = x % p.n_pairs;
+  x /= p.n_pairs;
+  it.chunk = x % p.n_chunks;
+  it.b = p.order[x / p.n_chunks];
+  it.rt = 2 * pair_idx + (int)sub;
+  it.y = layout_of(p, it.b);
+  if (it.y.T == 0) {   // capacity exceeded: nothing is computed for this request
+    it.tb = it.te = 0;
+    if (threadIdx.x == 0) record_error(p.status, TV_ERR_CAPACITY);
+    return true;
+  }
+  it.tb = (int)((int64_t)it.y.T * it.chunk / p.n_chunks);
+  it.te = (int)((int64_t)it.y.T * (it.chunk + 1) / p.n_chunks);
+  return true;
+}
+
 // ---- ring of slots shared by a pair (the leader's full barriers count both CTAs' shares) ------
 struct Ring {
   uint8_t* base;
@@ -392,13 +419,14 @@ struct Ring {
 };
 
 // ---- producer (warp 0, lane 0 does the copies) -------------------------------------------------
-// Pair S: this CTA's half of every tile's K entries (N/2 rows), all 512 dims, in two slots of four
-// 64-dim slices.  Pair O: every entry of the tile for this CTA's 256 value columns, in two slots
-// (one per 256-column group of O) of two 64-column blocks; rows past the tile's entry count
-// rounded up to 64 are not loaded.
+// Pair S: per item, its Q rows (eight 64-dim slices, two per slot) through the four ring slots on
+// this CTA's own q_tma barrier (these fills complete the slots' full barriers without bytes), then
+// this CTA's half of every tile's K entries (N/2 rows), all 512 dims, in two slots of four 64-dim
+// slices.  Pair O: every entry of each tile for this CTA's 256 value columns, in two slots (one
+// per 256-column group of O) of two 64-column blocks; rows past the tile's entry count rounded up
+// to 64 are not loaded.
 template <bool kPaged>
-__device__ void producer(const Params& p, Smem& sm, int b, int rt, bool role_s, uint32_t sub,
-                         const Layout& y, int tb, int te) {
+__device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
   const int lane = threadIdx.x & 31;
   const uint32_t leader = cluster_rank() & ~1u;
   Ring r{role_s ? sm.buf : sm.buf + 2 * kPBuf, role_s ? kSSlots : kOSlots, 0, 0};
@@ -425,99 +453,116 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, bool role_s, 
     issued_phase[r.slot] = r.phase;
     r.advance();
   };
-  const int tree_row = b * p.D;
   bool ok = true;
-  // tile rows are computed one tile ahead, so that with paged pools the page-table reads are in
-  // flight while the producer waits for slots
-  auto row_of = [&](int t) -> int2 {
-    int2 rw = make_int2(0, 0);
-    if (t < tb || t >= te) return rw;
-    const Tile x = tile_of(y, t);
-    if (x.kind == kExtra) return rw;
+  int q = 0;   // non-empty items so far
+  Item it;
+  for (int k = 0; ok && item_at(p, k, sub, it); ++k) {
+    if (it.tb >= it.te) continue;
+    const int b = it.b;
+    const Layout& y = it.y;
+    const int tree_row = b * p.D;
+    // pair O: the previous item's epilogue stages O in the V ring; its slots are free again
+    // once the role warps report v_free
+    if (!role_s && q > 0 && !mbar_wait(&sm.h.v_free, (q - 1) & 1, &sm.h.abort, p.timeout_ns)) {
+      if (lane == 0) fail(sm, p.status);
+      break;
+    }
+    ++q;
     if (role_s) {
-      rw.x = (int)tile_row<kPaged>(p, x.kind, b, x.row0 + (int)sub * (x.nqk / 2), y.t0);
-    } else {
-      rw.x = (int)tile_row<kPaged>(p, x.kind, b, x.row0, y.t0);
-      rw.y = kPaged ? (int)tile_row<kPaged>(p, x.kind, b, x.row0 + 64, y.t0) : rw.x + 64;
-    }
-    return rw;
-  };
-  if (role_s) {
-    // Q of this CTA's 128 rows (8 slices of 64 dims, 16 KB each) arrives first, in the four ring
-    // slots, on this CTA's own barrier; the softmax warps move it into TMEM and the leader's MMA
-    // issuer then releases the slots.  These four fills complete the slots' first full phase
-    // without bytes.
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&sm.h.q_tma, 8 * 16384);
-      for (int s = 0; s < 8; ++s)
-        tma_load_3d(sm.buf + s * 16384, &p.mQ, 64 * s, 128 * rt, b, &sm.h.q_tma);
-      if (sub == 0)
-        for (int i = 0; i < kSSlots; ++i) mbar_arrive(&sm.h.full[i]);
-    }
-    for (int i = 0; i < kSSlots; ++i) finish(false);
-  }
-  int2 cur = row_of(tb);
-  for (int t = tb; t < te && ok; ++t) {
-    const int2 next = row_of(t + 1);
-    const Tile x = tile_of(y, t);
-    for (int g = 0; g < 2 && ok; ++g) {
-      if (!acquire()) {
-        ok = false;
-        break;
+      for (int j = 0; j < kSSlots && ok; ++j) {
+        if (!acquire()) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (j == 0) mbar_arrive_expect_tx(&sm.h.q_tma, 8 * 16384);
+          for (int s = 2 * j; s < 2 * j + 2; ++s)
+            tma_load_3d(r.base + r.slot * kSlotBytes + (s & 1) * 16384, &p.mQ, 64 * s,
+                        128 * it.rt, b, &sm.h.q_tma);
+          if (sub == 0) mbar_arrive(&sm.h.full[r.slot]);
+        }
+        finish(false);
       }
-      uint8_t* dst = r.base + r.slot * kSlotBytes;
-      const uint32_t bar = leader_full();
-      bool loads = true;
+    }
+    // tile rows are computed one tile ahead, so that with paged pools the page-table reads are
+    // in flight while the producer waits for slots
+    auto row_of = [&](int t) -> int2 {
+      int2 rw = make_int2(0, 0);
+      if (t < it.tb || t >= it.te) return rw;
+      const Tile x = tile_of(y, t);
+      if (x.kind == kExtra) return rw;
       if (role_s) {
-        loads = t != p.withhold_tile;   // test aid: the MMA issuer's wait for it runs out
-        if (lane == 0 && loads) {
-          if (x.kind == kExtra) {
-            // leader: tree rows | C4 scratch rows; follower: C128 scratch rows | zero rows
-            expect(kKSlices * 2 * kDp * 128);
-            for (int ks = 0; ks < kKSlices; ++ks) {
-              const int xcol = 64 * (kKSlices * g + ks);
-              uint8_t* d = dst + ks * 8192;
-              if (sub == 0) {
-                tma_load_2d_pair(d, &p.mTreeK, xcol, tree_row, bar);
-                tma_load_2d_pair(d + kDp * 128, &p.mS4K, xcol, tree_row, bar);
-              } else {
-                tma_load_2d_pair(d, &p.mS128K, xcol, tree_row, bar);
-                tma_load_2d_pair(d + kDp * 128, &p.mTreeK, xcol, p.tree_rows, bar);
+        rw.x = (int)tile_row<kPaged>(p, x.kind, b, x.row0 + (int)sub * (x.nqk / 2), y.t0);
+      } else {
+        rw.x = (int)tile_row<kPaged>(p, x.kind, b, x.row0, y.t0);
+        rw.y = kPaged ? (int)tile_row<kPaged>(p, x.kind, b, x.row0 + 64, y.t0) : rw.x + 64;
+      }
+      return rw;
+    };
+    int2 cur = row_of(it.tb);
+    for (int t = it.tb; t < it.te && ok; ++t) {
+      const int2 next = row_of(t + 1);
+      const Tile x = tile_of(y, t);
+      for (int g = 0; g < 2 && ok; ++g) {
+        if (!acquire()) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = r.base + r.slot * kSlotBytes;
+        const uint32_t bar = leader_full();
+        bool loads = true;
+        if (role_s) {
+          loads = t != p.withhold_tile;   // test aid: the MMA issuer's wait for it runs out
+          if (lane == 0 && loads) {
+            if (x.kind == kExtra) {
+              // leader: tree rows | C4 scratch rows; follower: C128 scratch rows | zero rows
+              expect(kKSlices * 2 * kDp * 128);
+              for (int ks = 0; ks < kKSlices; ++ks) {
+                const int xcol = 64 * (kKSlices * g + ks);
+                uint8_t* d = dst + ks * 8192;
+                if (sub == 0) {
+                  tma_load_2d_pair(d, &p.mTreeK, xcol, tree_row, bar);
+                  tma_load_2d_pair(d + kDp * 128, &p.mS4K, xcol, tree_row, bar);
+                } else {
+                  tma_load_2d_pair(d, &p.mS128K, xcol, tree_row, bar);
+                  tma_load_2d_pair(d + kDp * 128, &p.mTreeK, xcol, p.tree_rows, bar);
+                }
               }
+            } else {
+              const CUtensorMap* m =
+                  x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
+              expect(kSlotBytes);
+              for (int ks = 0; ks < kKSlices; ++ks)
+                tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * g + ks), cur.x, bar);
+            }
+          }
+        } else if (lane == 0) {
+          const int col0 = 256 * g + 128 * (int)sub;
+          if (x.kind == kExtra) {
+            expect(2 * 4 * kDp * 128);
+            for (int cb = 0; cb < 2; ++cb) {
+              uint8_t* d = dst + cb * kVBlock;
+              const int xc = col0 + 64 * cb;
+              tma_load_2d_pair(d, &p.mTreeV, xc, tree_row, bar);
+              tma_load_2d_pair(d + kDp * 128, &p.mS4V, xc, tree_row, bar);
+              tma_load_2d_pair(d + 2 * kDp * 128, &p.mS128V, xc, tree_row, bar);
+              tma_load_2d_pair(d + 3 * kDp * 128, &p.mTreeV, xc, p.tree_rows, bar);   // zeros
             }
           } else {
             const CUtensorMap* m =
-                x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
-            expect(kSlotBytes);
-            for (int ks = 0; ks < kKSlices; ++ks)
-              tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * g + ks), cur.x, bar);
+                x.kind == kC4 ? &p.mC4V : x.kind == kC128 ? &p.mC128V : &p.mRawV;
+            const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
+            expect(nvh * 2 * 8192);
+            for (int h = 0; h < nvh; ++h)
+              for (int cb = 0; cb < 2; ++cb)
+                tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb,
+                                 h == 0 ? cur.x : cur.y, bar);
           }
         }
-      } else if (lane == 0) {
-        const int col0 = 256 * g + 128 * (int)sub;
-        if (x.kind == kExtra) {
-          expect(2 * 4 * kDp * 128);
-          for (int cb = 0; cb < 2; ++cb) {
-            uint8_t* d = dst + cb * kVBlock;
-            const int xc = col0 + 64 * cb;
-            tma_load_2d_pair(d, &p.mTreeV, xc, tree_row, bar);
-            tma_load_2d_pair(d + kDp * 128, &p.mS4V, xc, tree_row, bar);
-            tma_load_2d_pair(d + 2 * kDp * 128, &p.mS128V, xc, tree_row, bar);
-            tma_load_2d_pair(d + 3 * kDp * 128, &p.mTreeV, xc, p.tree_rows, bar);   // zeros
-          }
-        } else {
-          const CUtensorMap* m = x.kind == kC4 ? &p.mC4V : x.kind == kC128 ? &p.mC128V : &p.mRawV;
-          const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
-          expect(nvh * 2 * 8192);
-          for (int h = 0; h < nvh; ++h)
-            for (int cb = 0; cb < 2; ++cb)
-              tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb,
-                               h == 0 ? cur.x : cur.y, bar);
-        }
+        finish(loads);
       }
-      finish(loads);
+      cur = next;
     }
-    cur = next;
   }
   // drain: no copy issued by the pair may still be in flight when the CTA exits (the leader's
   // full barriers count both CTAs' shares; the closing cluster barrier covers the follower)
@@ -532,7 +577,8 @@ __device__ void producer(const Params& p, Smem& sm, int b, int rt, bool role_s, 
 // One thread issues every MMA of a pair, and a tcgen05.mma is accepted only about as fast as the
 // issuing thread reaches it: the instructions between two MMAs are not hidden behind the tensor
 // pipe.  So descriptors are built once, each MMA adds a compile-time offset, and the K-step loops
-// are unrolled without run-time branches.
+// are unrolled without run-time branches.  Tile counters run across items, so the parities of the
+// per-tile barriers and buffers continue from one item to the next.
 __device__ __forceinline__ bool wait_ring(const Params& p, Smem& sm, const Ring& r) {
   if (!mbar_wait(&sm.h.full[r.slot], r.phase, &sm.h.abort, p.timeout_ns)) {
     fail(sm, p.status);
@@ -544,34 +590,41 @@ __device__ __forceinline__ bool wait_ring(const Params& p, Smem& sm, const Ring&
 
 // Pair S: S_t = Q K_t^T into S buffer t & 1 (M = 256, N = the tile's entries, K = 512: A = Q from
 // TMEM columns [256, 512), B = K from the ring).
-__device__ void mma_s(const Params& p, Smem& sm, const Layout& y, int tb, int te) {
+__device__ void mma_s(const Params& p, Smem& sm) {
   const uint32_t tmem = sm.h.tmem;
   const uint16_t pair = 0x3;
   Ring r{sm.buf, kSSlots, 0, 0};
-  if (!mbar_wait(&sm.h.q_full, 0, &sm.h.abort, p.timeout_ns)) {
-    fail(sm, p.status);
-  } else {
+  const uint64_t ring_desc = smem_desc_sw128(smem_u32(sm.buf), 16, 1024);
+  int g = 0, q = 0;   // tiles and non-empty items so far
+  bool ok = true;
+  Item it;
+  for (int k = 0; ok && item_at(p, k, 0, it); ++k) {
+    const int n = it.te - it.tb;
+    if (n <= 0) continue;
+    if (!mbar_wait(&sm.h.q_full, q & 1, &sm.h.abort, p.timeout_ns)) {
+      fail(sm, p.status);
+      break;
+    }
     tc_fence_after();
+    ++q;
     // Q is in both CTAs' TMEM: the ring slots that carried it go back to the producers
     for (int i = 0; i < kSSlots; ++i) {
       mma2_commit_mc(&sm.h.empty[r.slot], pair);
       r.advance();
     }
-    const uint64_t ring_desc = smem_desc_sw128(smem_u32(sm.buf), 16, 1024);
-    const int n = te - tb;
-    for (int i = 0; i < n; ++i) {
-      const Tile x = tile_of(y, tb + i);
+    for (int i = 0; i < n && ok; ++i, ++g) {
+      const Tile x = tile_of(it.y, it.tb + i);
       const uint32_t idS = idesc_bf16_f32(256, x.nqk, 0, 0);
-      const uint32_t d_s = tmem + 128 * (i & 1);
-      // both CTAs' softmax warps have read S_{i-2} out of this buffer
-      if (i >= 2 && !mbar_wait(&sm.h.s_free[i & 1], ((i - 2) >> 1) & 1, &sm.h.abort,
-                               p.timeout_ns)) {
+      const uint32_t d_s = tmem + 128 * (g & 1);
+      // both CTAs' softmax warps have read S_{g-2} out of this buffer
+      if (g >= 2 &&
+          !mbar_wait(&sm.h.s_free[g & 1], ((g - 2) >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
         fail(sm, p.status);
+        ok = false;
         break;
       }
-      bool ok = true;
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
+      for (int h = 0; h < 2; ++h) {
         if (!wait_ring(p, sm, r)) {
           ok = false;
           break;
@@ -579,13 +632,13 @@ __device__ void mma_s(const Params& p, Smem& sm, const Layout& y, int tb, int te
         const uint64_t kd = desc_add(ring_desc, (uint32_t)r.slot * kSlotBytes);
 #pragma unroll
         for (int m = 0; m < 4 * kKSlices; ++m)
-          mma2_ts(d_s, tmem + kTmemQ + 8 * (4 * kKSlices * g + m),
-                  desc_add(kd, (m >> 2) * 8192 + 32 * (m & 3)), idS, (g | m) ? 1u : 0u);
+          mma2_ts(d_s, tmem + kTmemQ + 8 * (4 * kKSlices * h + m),
+                  desc_add(kd, (m >> 2) * 8192 + 32 * (m & 3)), idS, (h | m) ? 1u : 0u);
         mma2_commit_mc(&sm.h.empty[r.slot], pair);
         r.advance();
       }
       if (!ok) break;
-      mma2_commit_mc(&sm.h.s_full[i & 1], pair);
+      mma2_commit_mc(&sm.h.s_full[g & 1], pair);
     }
   }
   // drain every MMA this thread issued before TMEM is released
@@ -594,120 +647,155 @@ __device__ void mma_s(const Params& p, Smem& sm, const Layout& y, int tb, int te
   mbar_wait(&sm.h.drain, 0, &never, p.timeout_ns / 4);
 }
 
-// Pair O: O[:, 256g .. 256g+255] += P_t V_t[:, 256g .. 256g+255] for g = 0, 1 (M = 256, N = 256,
-// K = the tile's entries: A = P from the P buffer of parity t, B = V from the ring).
-__device__ void mma_o(const Params& p, Smem& sm, const Layout& y, int tb, int te) {
+// Pair O: O[:, 256j .. 256j+255] += P_t V_t[:, 256j .. 256j+255] for j = 0, 1 (M = 256, N = 256,
+// K = the tile's entries: A = P from the P buffer of parity t, B = V from the ring).  An item's
+// first PV waits until the previous item's O has left TMEM.
+__device__ void mma_o(const Params& p, Smem& sm) {
   const uint32_t tmem = sm.h.tmem;
   const uint16_t pair = 0xC, pair_s = 0x3;
   Ring r{sm.buf + 2 * kPBuf, kOSlots, 0, 0};
   const uint64_t p_desc = smem_desc_sw128(smem_u32(sm.buf), 16, 1024);
   const uint64_t ring_desc = smem_desc_sw128(smem_u32(r.base), kVBlock, 1024);
   const uint32_t idO = idesc_bf16_f32(256, 256, 0, 1);
-  const int n = te - tb;
+  int g = 0, q = 0;
   bool ok = true;
-  for (int i = 0; i < n && ok; ++i) {
-    const Tile x = tile_of(y, tb + i);
-    const int nks = x.nqk / 16;
-    if (!mbar_wait(&sm.h.p_full[i & 1], (i >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
+  Item it;
+  for (int k = 0; ok && item_at(p, k, 0, it); ++k) {
+    const int n = it.te - it.tb;
+    if (n <= 0) continue;
+    if (q > 0 && !mbar_wait(&sm.h.o_free, (q - 1) & 1, &sm.h.abort, p.timeout_ns)) {
       fail(sm, p.status);
-      ok = false;
       break;
     }
-    tc_fence_after();
-    // P of this tile: two 64-entry panels of 128 rows x 128 B (K-major, 128-byte swizzle)
-    const uint64_t pd = desc_add(p_desc, (uint32_t)(i & 1) * kPBuf);
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      if (!wait_ring(p, sm, r)) {
+    for (int i = 0; i < n && ok; ++i, ++g) {
+      const Tile x = tile_of(it.y, it.tb + i);
+      const int nks = x.nqk / 16;
+      if (!mbar_wait(&sm.h.p_full[g & 1], (g >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
+        fail(sm, p.status);
         ok = false;
         break;
       }
-      const uint64_t vd = desc_add(ring_desc, (uint32_t)r.slot * kSlotBytes);
-      const uint32_t od = tmem + 256 * g;
-      if (nks == 8) {
-        mma2_ss(od, pd, vd, idO, i > 0 ? 1u : 0u);
+      tc_fence_after();
+      // P of this tile: two 64-entry panels of 128 rows x 128 B (K-major, 128-byte swizzle)
+      const uint64_t pd = desc_add(p_desc, (uint32_t)(g & 1) * kPBuf);
 #pragma unroll
-        for (int ks = 1; ks < 8; ++ks)
-          mma2_ss(od, desc_add(pd, (ks >> 2) * 16384 + 32 * (ks & 3)), desc_add(vd, 2048 * ks),
-                  idO, 1u);
-      } else {
-        for (int ks = 0; ks < nks; ++ks)
-          mma2_ss(od, desc_add(pd, (ks >> 2) * 16384 + 32 * (ks & 3)), desc_add(vd, 2048 * ks),
-                  idO, (i > 0 || ks > 0) ? 1u : 0u);
+      for (int j = 0; j < 2; ++j) {
+        if (!wait_ring(p, sm, r)) {
+          ok = false;
+          break;
+        }
+        const uint64_t vd = desc_add(ring_desc, (uint32_t)r.slot * kSlotBytes);
+        const uint32_t od = tmem + 256 * j;
+        if (nks == 8) {
+          mma2_ss(od, pd, vd, idO, i > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 1; ks < 8; ++ks)
+            mma2_ss(od, desc_add(pd, (ks >> 2) * 16384 + 32 * (ks & 3)),
+                    desc_add(vd, 2048 * ks), idO, 1u);
+        } else {
+          for (int ks = 0; ks < nks; ++ks)
+            mma2_ss(od, desc_add(pd, (ks >> 2) * 16384 + 32 * (ks & 3)),
+                    desc_add(vd, 2048 * ks), idO, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma2_commit_mc(&sm.h.empty[r.slot], pair);
+        r.advance();
       }
-      mma2_commit_mc(&sm.h.empty[r.slot], pair);
-      r.advance();
+      if (!ok) break;
+      mma2_commit_mc(&sm.h.pv_done, pair);
+      mma2_commit_mc(&sm.h.p_free[g & 1], pair_s);   // pair S may overwrite this P buffer
     }
     if (!ok) break;
-    mma2_commit_mc(&sm.h.pv_done, pair);
-    mma2_commit_mc(&sm.h.p_free[i & 1], pair_s);   // pair S may overwrite this P buffer
+    mma2_commit_mc(&sm.h.o_full, pair);
+    ++q;
   }
-  if (ok) mma2_commit_mc(&sm.h.o_full, pair);
   mma2_commit_mc(&sm.h.drain, (uint16_t)(1u << cluster_rank()));
   volatile int never = 0;
   mbar_wait(&sm.h.drain, 0, &never, p.timeout_ns / 4);
 }
 
 // ---- signal warps (lane 0) -----------------------------------------------------------------------
-// Pair S: Q in this CTA's TMEM -> q_full; S_t read by this CTA's softmax warps -> s_free.
-// Pair O: tile t's rescale applied and P_t landed in this CTA -> p_full.  A follower cannot signal
-// tile t + 2 before the leader's barrier of tile t completed (the pipelines make the later signal
-// depend on the earlier one), so two parities suffice.
-// Pair S also moves P: once this CTA's softmax warps have staged P_t (and pair O's MMAs are done
-// with the destination buffer, the PV of tile t-2), one bulk copy takes the staged buffer to the
-// row partner's P buffer of parity t and completes its p_in barrier; the copy of P_t having read
-// its staging buffer frees that buffer for P_{t+2}.
-__device__ void signal_s(const Params& p, Smem& sm, int n, uint32_t rank) {
+// Pair S: Q in this CTA's TMEM -> q_full; S_t read by this CTA's softmax warps -> s_free; and the
+// P transfer: once this CTA's softmax warps have staged P_t (and pair O's MMAs are done with the
+// destination buffer, the PV of tile t-2), one bulk copy takes the staged buffer to the row
+// partner's P buffer of parity t and completes its p_in barrier; the copy of P_t having read its
+// staging buffer frees that buffer for P_{t+2}.
+// Pair O: tile t's rescale applied and P_t landed in this CTA -> p_full.
+// A follower cannot signal tile t + 2 before the leader's barrier of tile t completed (the
+// pipelines make the later signal depend on the earlier one), so two parities suffice.
+__device__ void signal_s(const Params& p, Smem& sm, uint32_t rank) {
   const uint32_t leader = rank & ~1u;
   const bool is_leader = (rank & 1u) == 0;
   const uint32_t partner = rank + 2;
-  if (!mbar_wait(&sm.h.q_local, 0, &sm.h.abort, p.timeout_ns)) {
-    fail(sm, p.status);
-    return;
-  }
-  signal_leader(sm, &sm.h.q_full, &sm.h.flag[0], is_leader, leader, 1u);
   const uint32_t dst0 = mapa_cluster(smem_u32(sm.buf), partner);
   const uint32_t bar0 = mapa_cluster(smem_u32(&sm.h.p_in[0]), partner);
   const uint32_t src0 = smem_u32(sm.buf + kSSlots * kSlotBytes);
-  for (int i = 0; i < n; ++i) {
-    const int sb = i & 1;
-    const uint32_t ph = (i >> 1) & 1;
-    if (!mbar_wait(&sm.h.s_read[sb], ph, &sm.h.abort, p.timeout_ns)) {
+  int g = 0, q = 0;
+  Item it;
+  for (int k = 0; item_at(p, k, rank & 1u, it); ++k) {
+    const int n = it.te - it.tb;
+    if (n <= 0) continue;
+    if (!mbar_wait(&sm.h.q_local, q & 1, &sm.h.abort, p.timeout_ns)) {
       fail(sm, p.status);
-      return;
+      break;
     }
-    signal_leader(sm, &sm.h.s_free[sb], &sm.h.flag[1 + sb], is_leader, leader, (uint32_t)i);
-    if (!mbar_wait(&sm.h.p_staged[sb], ph, &sm.h.abort, p.timeout_ns) ||
-        (i >= 2 && !mbar_wait(&sm.h.p_free[sb], ((i - 2) >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
+    ++q;
+    signal_leader(sm, &sm.h.q_full, &sm.h.flag[0], is_leader, leader, (uint32_t)q);
+    bool ok = true;
+    for (int i = 0; i < n; ++i, ++g) {
+      const int sb = g & 1;
+      const uint32_t ph = (g >> 1) & 1;
+      if (!mbar_wait(&sm.h.s_read[sb], ph, &sm.h.abort, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      signal_leader(sm, &sm.h.s_free[sb], &sm.h.flag[1 + sb], is_leader, leader, (uint32_t)g);
+      if (!mbar_wait(&sm.h.p_staged[sb], ph, &sm.h.abort, p.timeout_ns) ||
+          (g >= 2 && !mbar_wait(&sm.h.p_free[sb], ((g - 2) >> 1) & 1, &sm.h.abort,
+                                p.timeout_ns))) {
+        ok = false;
+        break;
+      }
+      asm volatile(
+          "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+          "[%3];" ::"r"(dst0 + (uint32_t)sb * kPBuf),
+          "r"(src0 + (uint32_t)sb * kPBuf), "r"((uint32_t)kPMsg), "r"(bar0 + (uint32_t)sb * 8)
+          : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      // the copy of P_{g-1} has read its staging buffer: P_{g+1} may be staged there
+      if (g >= 1) {
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        mbar_arrive(&sm.h.stage_free[sb ^ 1]);
+      }
+    }
+    if (!ok) {
       fail(sm, p.status);
-      return;
-    }
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];" ::"r"(dst0 + (uint32_t)sb * kPBuf),
-        "r"(src0 + (uint32_t)sb * kPBuf), "r"((uint32_t)kPMsg), "r"(bar0 + (uint32_t)sb * 8)
-        : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    // the copy of P_{i-1} has read its staging buffer: P_{i+1} may be staged there
-    if (i >= 1) {
-      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      mbar_arrive(&sm.h.stage_free[sb ^ 1]);
+      break;
     }
   }
   // every copy has read its source before the CTA moves on
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-__device__ void signal_o(const Params& p, Smem& sm, int n, uint32_t rank) {
+__device__ void signal_o(const Params& p, Smem& sm, uint32_t rank) {
   const uint32_t leader = rank & ~1u;
   const bool is_leader = (rank & 1u) == 0;
-  for (int i = 0; i < n; ++i) {
-    if (!mbar_wait(&sm.h.p_local[i & 1], (i >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
-      fail(sm, p.status);
-      return;
+  int g = 0;
+  Item it;
+  for (int k = 0; item_at(p, k, rank & 1u, it); ++k) {
+    const int n = it.te - it.tb;
+    bool ok = true;
+    for (int i = 0; i < n; ++i, ++g) {
+      if (!mbar_wait(&sm.h.p_local[g & 1], (g >> 1) & 1, &sm.h.abort, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      signal_leader(sm, &sm.h.p_full[g & 1], &sm.h.flag[1 + (g & 1)], is_leader, leader,
+                    (uint32_t)g);
     }
-    signal_leader(sm, &sm.h.p_full[i & 1], &sm.h.flag[1 + (i & 1)], is_leader, leader,
-                  (uint32_t)i);
+    if (!ok) {
+      fail(sm, p.status);
+      break;
+    }
   }
 }
 
@@ -719,317 +807,358 @@ __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
 
-__device__ void softmax_s(const Params& p, Smem& sm, int b, int rt, uint32_t rank, const Layout& y,
-                          int tb, int te) {
+__device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int ch = (warp - 2) >> 2;
   const int row = 32 * quad + lane;
-  const int grow = 128 * rt + row;
-  const bool row_ok = grow < p.DH;
   const uint32_t tmem = sm.h.tmem;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const float sl2 = p.scale_log2;
-  const int n = te - tb;
-
+  const uint32_t partner = rank + 2;
+  // this row's line in the P staging buffers (panel ch, 128-byte swizzle: 16-byte chunk c of the
+  // row at chunk c ^ (row & 7)); the signal warp copies each staged buffer to the row partner
+  // (the CTA of pair O with the same rows)
+  uint8_t* const p_line = sm.buf + kSSlots * kSlotBytes + ch * 16384 + (row >> 3) * 1024 +
+                          (row & 7) * 128;
+  int g = 0, q = 0;
   bool ok = true;
-  // Q dims 256ch .. 256ch+255 of this row into TMEM columns 256 + 128ch ..: column c holds dims
-  // 2c (low half) and 2c + 1, the A-operand layout of a kind::f16 MMA
-  {
-    // the producer's TMA put Q in the ring as 8 slices of 128 rows x 64 dims (128-byte swizzle:
-    // 16-byte chunk c of row r at chunk c ^ (r & 7)); this thread moves dims 256ch .. 256ch+255
-    // of its row (slices 4ch .. 4ch+3) into TMEM, 32 columns per slice
-    if (!__all_sync(0xffffffffu, mbar_wait(&sm.h.q_tma, 0, &sm.h.abort, p.timeout_ns))) {
+  Item it;
+  for (int k = 0; ok && item_at(p, k, rank & 1u, it); ++k) {
+    const int n = it.te - it.tb;
+    if (n <= 0) continue;
+    const int b = it.b;
+    const int grow = 128 * it.rt + row;
+    const bool row_ok = grow < p.DH;
+    const Layout& y = it.y;
+    // Q: the producer's TMA put this item's Q rows in the ring as eight slices of 128 rows x 64
+    // dims (128-byte swizzle), slices 2j and 2j+1 in the j-th slot after the ring position the
+    // item started at (2 slots per earlier tile, 4 per earlier item); this thread moves dims
+    // 256ch .. 256ch+255 of its row (slices 4ch .. 4ch+3) into TMEM columns 256 + 128ch .., where
+    // column c holds dims 2c (low half) and 2c + 1, the A-operand layout of a kind::f16 MMA
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.h.q_tma, q & 1, &sm.h.abort, p.timeout_ns))) {
       fail(sm, p.status);
       ok = false;   // the first tile's exchange lets the row's other warp leave too
     }
+    const int q_slot0 = (2 * g) % kSSlots;
 #pragma unroll 1
     for (int sl = 0; sl < 4 && ok; ++sl) {
-      const uint8_t* line = sm.buf + (4 * ch + sl) * 16384 + (row >> 3) * 1024 + (row & 7) * 128;
-      uint32_t q[32];
+      const int s = 4 * ch + sl;
+      const uint8_t* line = sm.buf + ((q_slot0 + (s >> 1)) % kSSlots) * kSlotBytes +
+                            (s & 1) * 16384 + (row >> 3) * 1024 + (row & 7) * 128;
+      uint32_t qv[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint4 v = *reinterpret_cast<const uint4*>(line + ((c ^ (row & 7)) << 4));
-        q[4 * c] = v.x;
-        q[4 * c + 1] = v.y;
-        q[4 * c + 2] = v.z;
-        q[4 * c + 3] = v.w;
+        qv[4 * c] = v.x;
+        qv[4 * c + 1] = v.y;
+        qv[4 * c + 2] = v.z;
+        qv[4 * c + 3] = v.w;
       }
-      tmem_st32(tmem + lane_base + kTmemQ + 128 * ch + 32 * sl, q);
+      tmem_st32(tmem + lane_base + kTmemQ + 128 * ch + 32 * sl, qv);
     }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
     if (lane == 0 && ok) mbar_arrive(&sm.h.q_local);
-  }
+    ++q;
 
-  // per-row visibility of the raw tail and of the extra tile
-  int raw_lo = 0;
-  uint32_t extra_mask = 0;   // bit j: entry j of the extra tile is visible
-  if (row_ok) {
-    const int v = grow / p.H;
-    const int64_t i = (int64_t)b * p.D + v;
-    const uint64_t an = p.anc[i];
-    raw_lo = p.raw_lo[i];
-    const uint64_t v4 = (p.comp_mask & TV_COMP_C4) ? p.vis4[i] : 0;
-    const uint64_t v128 = (p.comp_mask & TV_COMP_C128) ? p.vis128[i] : 0;
-    for (int u = 0; u < p.D; ++u) {
-      if ((an >> u) & 1ull) {
-        const int dep = __popcll(an & ((1ull << u) - 1ull));
-        if (y.L + dep >= raw_lo) extra_mask |= 1u << u;
+    // per-row visibility of the raw tail and of the extra tile
+    int raw_lo = 0;
+    uint32_t extra_mask = 0;   // bit j: entry j of the extra tile is visible
+    if (row_ok) {
+      const int v = grow / p.H;
+      const int64_t i = (int64_t)b * p.D + v;
+      const uint64_t an = p.anc[i];
+      raw_lo = p.raw_lo[i];
+      const uint64_t v4 = (p.comp_mask & TV_COMP_C4) ? p.vis4[i] : 0;
+      const uint64_t v128 = (p.comp_mask & TV_COMP_C128) ? p.vis128[i] : 0;
+      for (int u = 0; u < p.D; ++u) {
+        if ((an >> u) & 1ull) {
+          const int dep = __popcll(an & ((1ull << u) - 1ull));
+          if (y.L + dep >= raw_lo) extra_mask |= 1u << u;
+        }
+        if ((v4 >> u) & 1ull) extra_mask |= 1u << (kDp + u);
+        if ((v128 >> u) & 1ull) extra_mask |= 1u << (2 * kDp + u);
       }
-      if ((v4 >> u) & 1ull) extra_mask |= 1u << (kDp + u);
-      if ((v128 >> u) & 1ull) extra_mask |= 1u << (2 * kDp + u);
     }
-  }
 
-  // this row's line in the P staging buffers (panel ch, 128-byte swizzle: 16-byte chunk c of the
-  // row at chunk c ^ (row & 7)); the signal warp copies each staged buffer to the row partner (the
-  // CTA of pair O with the same rows)
-  const uint32_t partner = rank + 2;
-  uint8_t* const p_line = sm.buf + kSSlots * kSlotBytes + ch * 16384 + (row >> 3) * 1024 +
-                          (row & 7) * 128;
-
-  float m_ref = -INFINITY, l_run = 0.f;
-  // The two warps of a row (column halves) meet at one named barrier per tile.  A warp whose
-  // bounded wait ran out still takes each barrier until both warps leave the tile loop together
-  // (each tile's exchange carries both warps' flags), so neither waits on the other forever.
-  for (int i = 0; i < n; ++i) {
-    const Tile x = tile_of(y, tb + i);
-    const int sb = i & 1;
-    const int c0 = 64 * ch;   // first S column of this thread
-    if (ok && !__all_sync(0xffffffffu,
-                          mbar_wait(&sm.h.s_full[sb], (i >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
-      fail(sm, p.status);
-      ok = false;
-    }
-    float s[64];
-    float raw_max = -INFINITY;
-    if (ok) {
-      tc_fence_after();
-      {
-        uint32_t* sr = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          if (c0 + 32 * c < x.nqk)
-            tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32 * c,
-                      *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-        tmem_wait_ld();
+    float m_ref = -INFINITY, l_run = 0.f;
+    // The two warps of a row (column halves) meet at one named barrier per tile.  A warp whose
+    // bounded wait ran out still takes each barrier until both warps leave the tile loop together
+    // (each tile's exchange carries both warps' flags), so neither waits on the other forever.
+    for (int i = 0; i < n; ++i, ++g) {
+      const Tile x = tile_of(y, it.tb + i);
+      const int sb = g & 1;
+      const int c0 = 64 * ch;   // first S column of this thread
+      if (ok && !__all_sync(0xffffffffu, mbar_wait(&sm.h.s_full[sb], (g >> 1) & 1, &sm.h.abort,
+                                                   p.timeout_ns))) {
+        fail(sm, p.status);
+        ok = false;
       }
-      // S_t is in registers: its buffer may take S_{t+2}
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.h.s_read[sb]);
-      // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
-      float mx[8];
+      float s[64];
+      float raw_max = -INFINITY;
+      if (ok) {
+        tc_fence_after();
+        {
+          uint32_t* sr = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-      const bool full_tile = (x.kind == kC4 || x.kind == kC128) && x.valid >= 128;
-      if (full_tile) {
+          for (int c = 0; c < 2; ++c)
+            if (c0 + 32 * c < x.nqk)
+              tmem_ld32(tmem + lane_base + 128 * sb + c0 + 32 * c,
+                        *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+          tmem_wait_ld();
+        }
+        // S_t is in registers: its buffer may take S_{t+2}
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.h.s_read[sb]);
+        // visible columns of this thread as a 64-bit mask: a range [lo, hi) of the tile's
+        // entries (prefix tiles: all valid entries; raw tiles: positions >= raw_lo), or the
+        // extra tile's per-node bits.  One code path for every tile kind.
+        uint64_t vmask;
+        if (x.kind == kExtra) {
+          vmask = c0 == 0 ? (uint64_t)extra_mask : 0ull;
+        } else {
+          const int hi = min(64, max(0, x.valid - c0));
+          const int lo = x.kind == kRaw ? min(hi, max(0, raw_lo - x.row0 - c0)) : 0;
+          vmask = (hi == 64 ? ~0ull : ((1ull << hi) - 1ull)) & ~((1ull << lo) - 1ull);
+        }
+        const uint32_t vlo = (uint32_t)vmask, vhi = (uint32_t)(vmask >> 32);
+        // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
+        float mx[8];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-      } else {
+        for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          const int col = c0 + j;
-          bool vis = col < x.valid;
-          if (x.kind == kRaw) vis = vis && (x.row0 + col >= raw_lo);
-          if (x.kind == kExtra) vis = col < kExtraEntries && ((extra_mask >> (col & 31)) & 1u);
+          const bool vis = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
           s[j] = vis ? s[j] : -INFINITY;
           mx[j & 7] = fmaxf(mx[j & 7], s[j]);
         }
+        raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       }
-      raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      sm.h.xmax[sb][ch][row] = raw_max;
+      if (lane == 0) sm.h.xok[sb][ch][quad] = ok ? 1 : 0;
+      pair_sync(quad);
+      raw_max = fmaxf(raw_max, sm.h.xmax[sb][ch ^ 1][row]);
+      if (ok && !sm.h.xok[sb][ch ^ 1][quad]) {   // the row's other warp gave up
+        fail(sm, p.status);
+        ok = false;
+      }
+      if (!ok) break;
+      const float mt = raw_max * sl2;
+      const bool grow_max = mt > m_ref + kRescaleThreshold;
+      const float m_new = grow_max ? mt : m_ref;
+      // exactly 1 unless the maximum grows past a finite reference: pair O rescales O by it
+      const float alpha = (grow_max && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
+      const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
+      float sum[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sum[j] = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg_m));
+        sum[j & 3] += p0 + p1;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const float tsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      l_run = l_run * alpha + tsum;
+      m_ref = m_new;
+      // the copy of P_{g-2} has read this staging buffer
+      if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sm.h.stage_free[sb], ((g - 2) >> 1) & 1,
+                                                       &sm.h.abort, p.timeout_ns))) {
+        fail(sm, p.status);
+        ok = false;
+        continue;   // the next tile's exchange lets the row's other warp leave too
+      }
+      uint8_t* const line = p_line + sb * kPBuf;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      if (ch == 0)
+        reinterpret_cast<float*>(sm.buf + kSSlots * kSlotBytes + sb * kPBuf + kPBytes)[row] =
+            alpha;
+      // the copy reads the staging buffer through the async proxy
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.h.p_staged[sb]);
     }
-    sm.h.xmax[sb][ch][row] = raw_max;
-    if (lane == 0) sm.h.xok[sb][ch][quad] = ok ? 1 : 0;
+    // combine the two partial row sums (both threads of a row share m_ref); both warps of a row
+    // take this barrier, whatever happened in the tile loop
+    sm.h.xsum[ch][row] = l_run;
+    if (lane == 0) sm.h.xok_end[ch][quad] = ok ? 1 : 0;
     pair_sync(quad);
-    raw_max = fmaxf(raw_max, sm.h.xmax[sb][ch ^ 1][row]);
-    if (ok && !sm.h.xok[sb][ch ^ 1][quad]) {   // the row's other warp gave up
-      fail(sm, p.status);
-      ok = false;
-    }
+    const float l_tot = l_run + sm.h.xsum[ch ^ 1][row];
+    ok = ok && sm.h.xok_end[ch ^ 1][quad];   // both warps of the row leave together
+    pair_sync(quad);   // both have read xsum before the next item overwrites it
     if (!ok) break;
-    const float mt = raw_max * sl2;
-    const bool grow_max = mt > m_ref + kRescaleThreshold;
-    const float m_new = grow_max ? mt : m_ref;
-    // exactly 1 unless the maximum grows past a finite reference: pair O rescales O by it
-    const float alpha = (grow_max && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-    const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
-    float sum[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) sum[k] = 0.f;
-    uint32_t pk[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg_m));
-      const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg_m));
-      sum[j & 3] += p0 + p1;
-      const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-      pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+    if (ch == 0) {
+      const int mb = (q - 1) & 1;
+      st_async_v2(mapa_cluster(smem_u32(&sm.h.ml[mb][row][0]), partner), __float_as_uint(m_ref),
+                  __float_as_uint(l_tot), mapa_cluster(smem_u32(&sm.h.ml_full[mb]), partner));
+      if (row_ok && p.n_chunks == 1)
+        p.lse[(int64_t)b * p.DH + grow] =
+            l_tot > 0.f ? (m_ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
     }
-    const float tsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
-    l_run = l_run * alpha + tsum;
-    m_ref = m_new;
-    // the copy of P_{i-2} has read this staging buffer
-    if (i >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sm.h.stage_free[sb], ((i - 2) >> 1) & 1,
-                                                     &sm.h.abort, p.timeout_ns))) {
-      fail(sm, p.status);
-      ok = false;
-      continue;   // the next tile's exchange lets the row's other warp leave too
-    }
-    uint8_t* const line = p_line + sb * kPBuf;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    if (ch == 0)
-      reinterpret_cast<float*>(sm.buf + kSSlots * kSlotBytes + sb * kPBuf + kPBytes)[row] = alpha;
-    // the copy reads the staging buffer through the async proxy
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.h.p_staged[sb]);
-  }
-  // combine the two partial row sums (both threads of a row share m_ref); both warps of a row
-  // take this barrier, whatever happened in the tile loop
-  sm.h.xsum[ch][row] = l_run;
-  pair_sync(quad);
-  const float l_tot = l_run + sm.h.xsum[ch ^ 1][row];
-  if (!ok) return;
-  if (ch == 0) {
-    st_async_v2(mapa_cluster(smem_u32(&sm.h.ml[row][0]), partner), __float_as_uint(m_ref),
-                __float_as_uint(l_tot), mapa_cluster(smem_u32(&sm.h.ml_full), partner));
-    if (row_ok && p.n_chunks == 1)
-      p.lse[(int64_t)b * p.DH + grow] =
-          l_tot > 0.f ? (m_ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
   }
 }
 
-// ---- pair O role warps: per-tile rescale, then the epilogue --------------------------------------
+// ---- pair O role warps: per-tile rescale, then each item's epilogue ------------------------------
 // Warp w (2..9) serves lane quadrant w % 4 and O columns 256ch .. 256ch+255, ch = (w-2)/4.
-__device__ void rescale_epilogue_o(const Params& p, Smem& sm, int b, int rt, int chunk,
-                                   const Layout& y, int tb, int te) {
+__device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int ch = (warp - 2) >> 2;
   const int row = 32 * quad + lane;
-  const int grow = 128 * rt + row;
-  const bool row_ok = grow < p.DH;
   const uint32_t tmem = sm.h.tmem;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-  const int n = te - tb;
-  const bool arms = row == 0 && ch == 0;   // the thread that arms the per-tile barriers
-  bool ok = true;
-  for (int i = 0; i < n; ++i) {
-    const int sb = i & 1;
-    if (arms) mbar_arrive_expect_tx(&sm.h.p_in[sb], kPMsg);
-    if (!__all_sync(0xffffffffu,
-                    mbar_wait(&sm.h.p_in[sb], (i >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
-      fail(sm, p.status);
-      ok = false;
-      break;
+  const bool arms = row == 0 && ch == 0;   // the thread that arms the receiving barriers
+  const int d = 512;
+  int g = 0, q = 0;
+  Item it;
+  for (int k = 0; item_at(p, k, rank & 1u, it); ++k) {
+    const int n = it.te - it.tb;
+    const int b = it.b;
+    const int grow = 128 * it.rt + row;
+    const bool row_ok = grow < p.DH;
+    if (n <= 0) {
+      if (it.y.T > 0 && p.n_chunks > 1 && row_ok) {   // an empty KV chunk: l = 0
+        float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + it.chunk) * (d + 4);
+        for (int c = 0; c < 256; c += 4)
+          *reinterpret_cast<float4*>(prow + 256 * ch + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ch == 0) {
+          prow[d] = -INFINITY;
+          prow[d + 1] = 0.f;
+        }
+      }
+      continue;
     }
-    const float alpha = reinterpret_cast<const float*>(sm.buf + sb * kPBuf + kPBytes)[row];
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-      // O must hold every earlier PV before it is rescaled (tile 0 always sends 1)
+    const int mb = q & 1;
+    if (arms) mbar_arrive_expect_tx(&sm.h.ml_full[mb], 128 * 8);
+    for (int i = 0; i < n; ++i, ++g) {
+      const int sb = g & 1;
+      if (arms) mbar_arrive_expect_tx(&sm.h.p_in[sb], kPMsg);
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(&sm.h.pv_done, (i - 1) & 1, &sm.h.abort, p.timeout_ns))) {
+                      mbar_wait(&sm.h.p_in[sb], (g >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
         fail(sm, p.status);
-        ok = false;
-        break;
+        return;
       }
-      tc_fence_after();
+      const float alpha = reinterpret_cast<const float*>(sm.buf + sb * kPBuf + kPBytes)[row];
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        // O must hold every earlier PV of the item before it is rescaled (an item's first tile
+        // always sends 1)
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&sm.h.pv_done, (g - 1) & 1, &sm.h.abort, p.timeout_ns))) {
+          fail(sm, p.status);
+          return;
+        }
+        tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 256 / 32; ++c) {
-        uint32_t r[32];
-        const uint32_t col = tmem + lane_base + 256 * ch + 32 * c;
-        tmem_ld32(col, r);
-        tmem_wait_ld();
+        for (int c = 0; c < 256 / 32; ++c) {
+          uint32_t r[32];
+          const uint32_t col = tmem + lane_base + 256 * ch + 32 * c;
+          tmem_ld32(col, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-        tmem_st32(col, r);
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(col, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
       }
-      tmem_wait_st();
-      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.h.p_local[sb]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.h.p_local[sb]);
-  }
-  if (!ok) return;
-  float m = -INFINITY, l = 0.f;
-  if (n > 0) {
-    if (arms) mbar_arrive_expect_tx(&sm.h.ml_full, 128 * 8);
-    if (!__all_sync(0xffffffffu, mbar_wait(&sm.h.o_full, 0, &sm.h.abort, p.timeout_ns)) ||
-        !__all_sync(0xffffffffu, mbar_wait(&sm.h.ml_full, 0, &sm.h.abort, p.timeout_ns))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.h.o_full, q & 1, &sm.h.abort, p.timeout_ns)) ||
+        !__all_sync(0xffffffffu,
+                    mbar_wait(&sm.h.ml_full[mb], (q >> 1) & 1, &sm.h.abort, p.timeout_ns))) {
       fail(sm, p.status);
       return;
     }
+    ++q;
     tc_fence_after();
-    m = sm.h.ml[row][0];
-    l = sm.h.ml[row][1];
-  }
-  const int d = 512;
-  if (p.n_chunks == 1) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    // O leaves through shared memory and TMA stores: the V ring (idle once o_full has been
-    // observed) takes this CTA's 128 rows x 512 columns as eight 64-column boxes with the 128-byte
-    // swizzle; rows past D*H fall outside the map and are not stored
-    uint8_t* stage = sm.buf + 2 * kPBuf;
-    for (int c = 0; c < 256 / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + 256 * ch + 32 * c, r);
-      tmem_wait_ld();
-      uint32_t w[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * k]) * inv,
-                                                       __uint_as_float(r[2 * k + 1]) * inv);
-        w[k] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      const int col = 256 * ch + 32 * c;   // O column of w[0]
-      uint8_t* line = stage + (col >> 6) * 16384 + row * 128;
-      const int cc0 = (col & 63) >> 3;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(line + (((cc0 + q) ^ (row & 7)) << 4)) =
-            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.h.stage_full);
-    // a bounded wait, not a CTA barrier: a role warp that gave up earlier never arrives
-    if (warp == 2 && lane == 0 && mbar_wait(&sm.h.stage_full, 0, &sm.h.abort, p.timeout_ns)) {
-      for (int k = 0; k < 8; ++k)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                reinterpret_cast<uint64_t>(&p.mO)),
-            "r"(64 * k), "r"(128 * rt), "r"(b), "r"(smem_u32(stage + k * 16384))
-            : "memory");
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    }
-  } else {
-    float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + chunk) * (d + 4);
-    for (int c = 0; c < 256 / 32; ++c) {
-      uint32_t r[32];
-      if (n > 0) {
+    const float m = sm.h.ml[mb][row][0], l = sm.h.ml[mb][row][1];
+    if (p.n_chunks == 1) {
+      // O leaves through shared memory and TMA stores: the V ring (idle from o_full until this
+      // CTA's producer sees o_free) takes this CTA's 128 rows x 512 columns as eight 64-column
+      // boxes with the 128-byte swizzle (16-byte chunk c of a row at c ^ (row & 7)); rows past
+      // D*H fall outside the map and are not stored
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint8_t* stage = sm.buf + 2 * kPBuf;
+      for (int c = 0; c < 256 / 32; ++c) {
+        uint32_t r[32];
         tmem_ld32(tmem + lane_base + 256 * ch + 32 * c, r);
         tmem_wait_ld();
-      }
-      if (row_ok) {
-        float4* dst = reinterpret_cast<float4*>(prow + 256 * ch + 32 * c);
+        uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          dst[k] = n > 0 ? make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 16; ++j) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * inv,
+                                                         __uint_as_float(r[2 * j + 1]) * inv);
+          w[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        const int col = 256 * ch + 32 * c;   // O column of w[0]
+        uint8_t* line = stage + (col >> 6) * 16384 + row * 128;
+        const int cc0 = (col & 63) >> 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(line + (((cc0 + j) ^ (row & 7)) << 4)) =
+              make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      }
+      fence_proxy_async_smem();
+      // O is out of TMEM (the next item's PV may start) and staged
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.h.o_free);
+        mbar_arrive(&sm.h.stage_full);
+      }
+      // one thread stores the boxes once every warp has staged its rows (a bounded wait, not a
+      // CTA barrier: a warp that gave up never arrives), then frees the V ring
+      if (warp == 2 && lane == 0) {
+        if (!mbar_wait(&sm.h.stage_full, (q - 1) & 1, &sm.h.abort, p.timeout_ns)) {
+          fail(sm, p.status);
+          return;
+        }
+        for (int j = 0; j < 8; ++j)
+          asm volatile(
+              "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+                  "l"(reinterpret_cast<uint64_t>(&p.mO)),
+              "r"(64 * j), "r"(128 * it.rt), "r"(b), "r"(smem_u32(stage + j * 16384))
+              : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        mbar_arrive(&sm.h.v_free);
+      }
+      continue;
+    } else {
+      float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + it.chunk) * (d + 4);
+      for (int c = 0; c < 256 / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + 256 * ch + 32 * c, r);
+        tmem_wait_ld();
+        if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(prow + 256 * ch + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (row_ok && ch == 0) {
+        prow[d] = m;
+        prow[d + 1] = l;
       }
     }
-    if (row_ok && ch == 0) {
-      prow[d] = m;
-      prow[d + 1] = l;
-    }
+    // O is out of TMEM: the next item's PV may start; the V ring was not used
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.h.o_free);
+    if (warp == 2 && lane == 0) mbar_arrive(&sm.h.v_free);
   }
 }
 
@@ -1046,24 +1175,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grid: clusters of 4 consecutive CTAs; rank = 2 * (0: pair S, 1: pair O) + (row tile & 1)
+  // clusters of 4 consecutive CTAs; rank = 2 * (0: pair S, 1: pair O) + (row tile & 1)
   const uint32_t rank = blockIdx.x & 3;
   const bool role_s = rank < 2;
   const uint32_t sub = rank & 1;
-  int x = blockIdx.x >> 2;
-  const int pair_idx = x % p.n_pairs;
-  x /= p.n_pairs;
-  const int chunk = x % p.n_chunks;
-  const int b = p.order[x / p.n_chunks];
-  const int rt = 2 * pair_idx + (int)sub;
-
-  const Layout y = layout_of(p, b);   // identical in all four CTAs
-  if (y.T == 0) {
-    if (threadIdx.x == 0) record_error(p.status, TV_ERR_CAPACITY);
-    return;
-  }
-  const int tb = (int)((int64_t)y.T * chunk / p.n_chunks);
-  const int te = (int)((int64_t)y.T * (chunk + 1) / p.n_chunks);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSSlots; ++i) {
@@ -1083,18 +1198,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(&sm.h.p_in[i], 1);
       mbar_init(&sm.h.p_local[i], kSmxWarps);
       mbar_init(&sm.h.p_full[i], 1);
+      mbar_init(&sm.h.ml_full[i], 1);
     }
     mbar_init(&sm.h.pv_done, 1);
     mbar_init(&sm.h.o_full, 1);
-    mbar_init(&sm.h.ml_full, 1);
-    mbar_init(&sm.h.drain, 1);
+    mbar_init(&sm.h.o_free, kSmxWarps);
     mbar_init(&sm.h.stage_full, kSmxWarps);
+    mbar_init(&sm.h.v_free, 1);
+    mbar_init(&sm.h.drain, 1);
     sm.h.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(role_s ? &p.mC4K : &p.mC4V);
-    prefetch_tmap(role_s ? &p.mRawK : &p.mRawV);
+    prefetch_tmap(role_s ? &p.mQ : &p.mC4V);
+    prefetch_tmap(role_s ? &p.mC4K : &p.mRawV);
   }
   if (warp == 1) {
     tmem_alloc2(&sm.h.tmem, 512);
@@ -1104,32 +1221,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   cluster_sync();   // every CTA's barriers exist before any remote arrive, store or pair MMA
   tc_fence_after();
 
-  if (tb < te) {
-    if (warp == 0) {
-      producer<kPaged>(p, sm, b, rt, role_s, sub, y, tb, te);
-    } else if (warp == 1) {
-      if (lane == 0 && sub == 0) {
-        if (role_s)
-          mma_s(p, sm, y, tb, te);
-        else
-          mma_o(p, sm, y, tb, te);
-      }
-      __syncwarp();
-    } else if (warp == kSigWarp) {
-      if (lane == 0) {
-        if (role_s)
-          signal_s(p, sm, te - tb, rank);
-        else
-          signal_o(p, sm, te - tb, rank);
-      }
-      __syncwarp();
-    } else if (role_s) {
-      softmax_s(p, sm, b, rt, rank, y, tb, te);
-    } else {
-      rescale_epilogue_o(p, sm, b, rt, chunk, y, tb, te);
+  if (warp == 0) {
+    producer<kPaged>(p, sm, role_s, sub);
+  } else if (warp == 1) {
+    if (lane == 0 && sub == 0) {
+      if (role_s)
+        mma_s(p, sm);
+      else
+        mma_o(p, sm);
     }
-  } else if (warp >= 2 && warp < kSigWarp && !role_s) {
-    rescale_epilogue_o(p, sm, b, rt, chunk, y, tb, te);   // empty chunk: l = 0
+    __syncwarp();
+  } else if (warp == kSigWarp) {
+    if (lane == 0) {
+      if (role_s)
+        signal_s(p, sm, rank);
+      else
+        signal_o(p, sm, rank);
+    }
+    __syncwarp();
+  } else if (role_s) {
+    softmax_s(p, sm, rank);
+  } else {
+    rescale_epilogue_o(p, sm, rank);
   }
 
   tc_fence_before();
@@ -1438,7 +1551,10 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   if (cluster_slots() <= 0)
     return tv_check_launch("tv_tree_verify_attn (tcgen05 kernel attributes)");
   const size_t smem = sizeof(Smem);
-  const unsigned grid = (unsigned)(s->B * p.n_chunks * p.n_pairs * kClusterCtas);
+  // persistent clusters: one per resident cluster slot, at most one per work item
+  const int64_t items = (int64_t)s->B * p.n_chunks * p.n_pairs;
+  const int64_t clusters = items < cluster_slots() ? items : cluster_slots();
+  const unsigned grid = (unsigned)(clusters * kClusterCtas);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
