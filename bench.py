@@ -77,6 +77,10 @@ def parse():
     ap.add_argument("--draft", action="store_true",
                     help="draft-side tree attention instead of the bench line: per draft step of "
                          "a width-2 beam tree (B=64, serving cache geometry), one JSON line")
+    ap.add_argument("--cpu-baseline-only", action="store_true",
+                    help="print the oracle's CPU figure for the workload and exit (no GPU)")
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle work in the CPU figure")
     ap.add_argument("--cells", type=str, default=None,
                     help="with --sweep: comma-separated cell indices (default: all 64)")
     return ap.parse_args()
@@ -333,6 +337,33 @@ def cpu_threads():
     return os.cpu_count()
 
 
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
+
+
+def cpu_baseline_single_thread(args, budget_s=8.0):
+    """The same oracle sample with every BLAS / OpenMP pool limited to one thread (a child process,
+    since the limits must be set before numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--workload",
+           args.workload, "--cpu-budget", str(budget_s)]
+    if args.batch:
+        cmd += ["--batch", str(args.batch)]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
 def cpu_baseline(wl, budget_s=20.0):
     """Time the oracle's verify round on requests 0, 1, ... until ~budget_s of CPU work."""
     order = list(range(wl.B))
@@ -467,7 +498,24 @@ def run_ours(args, world, rank, local):
             step(args.warmup + k, ev[k])
     t_end.record(stream)
     torch.cuda.synchronize()
+    # clocks under load: the same rounds replayed back to back for ~1.5 s while the sampler runs
+    # (the timed steps alone last a few ms, too short for a 100 ms sampler)
+    t_load = time.perf_counter()
+    k = 0
+    while time.perf_counter() - t_load < 1.5:
+        for _ in range(50):
+            if graphs:
+                graphs[k % n_sets].replay()
+            else:
+                step(k)
+            k += 1
+        torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
+    if clk is not None:
+        clk["under_load"] = f"{k} rounds replayed back to back over {time.perf_counter() - t_load:.1f} s"
+    for st_, rb_, l0_ in sets:   # the replays committed rounds: back to the set's state
+        st_.L.copy_(l0_)
+    torch.cuda.synchronize()
     barrier(world)
     if graphs:
         for k in range(args.steps):
@@ -556,6 +604,23 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     barrier(world)
+    # the same end-to-end loop with the five C-ABI calls launched one by one every step (the host
+    # side of every call -- validation, tensor-map encoding, launches -- inside the timed region)
+    e2e_eager_ms = None
+    if graphs:
+        graphs_saved, graphs = graphs, None
+        e2e_run(args.warmup)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e3 = torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        e2e_run(args.steps, e2)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        e2e_eager_ms = max_over_ranks(e2.elapsed_time(e3) / args.steps, world)
+        graphs = graphs_saved
+        barrier(world)
     for k in range(min(args.steps, n_sets)):
         if int(host_out[k][0].min()) < 1:
             raise SystemExit("end-to-end step returned an accept length below 1")
@@ -603,11 +668,21 @@ def run_ours(args, world, rank, local):
                          "the round launched call by call") + " through the C ABI; inputs "
                         f"uploaded from pinned host memory one step ahead on {n_cs} copy "
                         "stream(s); acceptance results read back each step"},
+        "e2e_eager": None if e2e_eager_ms is None else {
+            "value": tokens_per_step / (e2e_eager_ms * 1e-3), "unit": "verified tree tokens/s",
+            "ms_per_step": e2e_eager_ms,
+            "note": "the same end-to-end loop with the five C-ABI calls launched call by call "
+                    "every step"},
         "gpu_launches": args.steps * launches_per_step(shape, tc_name),
         "clocks": clk,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"]["cpu_model"] = cpu_model()
+        one = cpu_baseline_single_thread(args)
+        if one is not None:
+            line["cpu_baseline"]["single_thread"] = {"value": one["value"], "cores": 1,
+                                                     "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -729,6 +804,10 @@ def launches_per_step(shape, kernel):
 
 def main():
     args = parse()
+    if args.cpu_baseline_only:
+        wl = make_workload(args.workload, 0, args.batch)
+        print(json.dumps(cpu_baseline(wl, args.cpu_budget)), flush=True)
+        return
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
         rank = int(os.environ.get("RANK", "0"))

@@ -65,7 +65,8 @@ constexpr int kSmxWarps = 8;                     // softmax / rescale warps, two
 constexpr int kSigWarp = 2 + kSmxWarps;          // forwards per-tile readiness to the pair leader
 constexpr int kThreads = 64 + 32 * kSmxWarps + 32;   // producer, MMA issuer, role warps, signal
 constexpr int kSlotBytes = 32768;
-constexpr int kSSlots = 4;      // pair S: K ring (a tile's K share is two slots of 4 x 64 dims)
+constexpr int kSSlots = 5;      // pair S: K ring (a tile's K share is two slots of 4 x 64 dims)
+constexpr int kQSlots = 4;      // pair S: an item's Q rows arrive through four ring slots
 constexpr int kOSlots = 4;      // pair O: V ring (a tile's V share is two slots of 128 columns)
 constexpr int kKSlices = 4;     // 64-dim K slices (64 entries x 128 B, 8 KB) per slot
 constexpr int kVBlock = 16384;  // V slot: two 64-column blocks of 128 entries
@@ -266,7 +267,7 @@ struct Header {
   uint64_t s_read[2];          // pair S: this CTA's softmax warps have read S_t (one per warp)
   uint64_t s_free[2];          // pair S (leader): both CTAs' softmax warps have read S_t
   uint64_t p_staged[2];        // pair S: this CTA's softmax warps have staged P_t (one per warp)
-  uint64_t stage_free[2];      // pair S: the copy of the staged P_{t-2} has read its buffer
+  uint64_t stage_free;         // pair S: the copy of the staged P_{t-1} has read the buffer
   uint64_t p_free[2];          // pair S: pair O's MMAs are done with the P buffer of parity t
   uint64_t p_in[2];            // pair O: the row partner's P_t and rescale factors have landed
   uint64_t p_local[2];         // pair O: this CTA's role warps have applied tile t's rescale
@@ -289,15 +290,16 @@ struct Header {
 };
 // A P buffer holds 128 rows x 128 entries of bf16 P as two 64-entry panels (K-major, 128-byte
 // swizzle), followed by the 128 rows' fp32 rescale factors.
+constexpr int kBufBytes = (kSSlots * kSlotBytes + kPBuf) > (2 * kPBuf + kOSlots * kSlotBytes)
+                              ? (kSSlots * kSlotBytes + kPBuf)
+                              : (2 * kPBuf + kOSlots * kSlotBytes);
 struct __align__(1024) Smem {
-  // pair S: the K ring (kSSlots x 32 KB, which also carries each item's Q), then two P staging
-  // buffers; pair O: two P buffers, then the V ring (kOSlots x 32 KB)
-  uint8_t buf[kSSlots * kSlotBytes + 2 * kPBuf];
+  // pair S: the K ring (kSSlots x 32 KB, which also carries each item's Q), then one P staging
+  // buffer; pair O: two P buffers, then the V ring (kOSlots x 32 KB)
+  uint8_t buf[kBufBytes];
   Header h;
 };
-static_assert(2 * kPBuf + kOSlots * kSlotBytes <= kSSlots * kSlotBytes + 2 * kPBuf,
-              "pair O buffers");
-static_assert(kSSlots * kSlotBytes == 8 * 16384, "an item's Q fills the K ring exactly");
+static_assert(kQSlots * kSlotBytes == 8 * 16384 && kQSlots <= kSSlots, "Q takes four K slots");
 static_assert(sizeof(Smem) <= 232448, "shared memory of one CTA exceeds the 227 KB limit");
 
 // 3-D tile load into this CTA's shared memory, completing this CTA's own mbarrier.
@@ -469,7 +471,7 @@ __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
     }
     ++q;
     if (role_s) {
-      for (int j = 0; j < kSSlots && ok; ++j) {
+      for (int j = 0; j < kQSlots && ok; ++j) {
         if (!acquire()) {
           ok = false;
           break;
@@ -608,7 +610,7 @@ __device__ void mma_s(const Params& p, Smem& sm) {
     tc_fence_after();
     ++q;
     // Q is in both CTAs' TMEM: the ring slots that carried it go back to the producers
-    for (int i = 0; i < kSSlots; ++i) {
+    for (int i = 0; i < kQSlots; ++i) {
       mma2_commit_mc(&sm.h.empty[r.slot], pair);
       r.advance();
     }
@@ -716,9 +718,9 @@ __device__ void mma_o(const Params& p, Smem& sm) {
 // ---- signal warps (lane 0) -----------------------------------------------------------------------
 // Pair S: Q in this CTA's TMEM -> q_full; S_t read by this CTA's softmax warps -> s_free; and the
 // P transfer: once this CTA's softmax warps have staged P_t (and pair O's MMAs are done with the
-// destination buffer, the PV of tile t-2), one bulk copy takes the staged buffer to the row
-// partner's P buffer of parity t and completes its p_in barrier; the copy of P_t having read its
-// staging buffer frees that buffer for P_{t+2}.
+// destination buffer, the PV of tile t-2), one bulk copy takes the staging buffer to the row
+// partner's P buffer of parity t and completes its p_in barrier; once the copy has read the
+// staging buffer, P_{t+1} may be staged there.
 // Pair O: tile t's rescale applied and P_t landed in this CTA -> p_full.
 // A follower cannot signal tile t + 2 before the leader's barrier of tile t completed (the
 // pipelines make the later signal depend on the earlier one), so two parities suffice.
@@ -758,14 +760,12 @@ __device__ void signal_s(const Params& p, Smem& sm, uint32_t rank) {
       asm volatile(
           "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
           "[%3];" ::"r"(dst0 + (uint32_t)sb * kPBuf),
-          "r"(src0 + (uint32_t)sb * kPBuf), "r"((uint32_t)kPMsg), "r"(bar0 + (uint32_t)sb * 8)
+          "r"(src0), "r"((uint32_t)kPMsg), "r"(bar0 + (uint32_t)sb * 8)
           : "memory");
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      // the copy of P_{g-1} has read its staging buffer: P_{g+1} may be staged there
-      if (g >= 1) {
-        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        mbar_arrive(&sm.h.stage_free[sb ^ 1]);
-      }
+      // the copy has read the staging buffer: P_{g+1} may be staged there
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      mbar_arrive(&sm.h.stage_free);
     }
     if (!ok) {
       fail(sm, p.status);
@@ -840,7 +840,7 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
       fail(sm, p.status);
       ok = false;   // the first tile's exchange lets the row's other warp leave too
     }
-    const int q_slot0 = (2 * g) % kSSlots;
+    const int q_slot0 = (kQSlots * q + 2 * g) % kSSlots;   // ring position at the item's start
 #pragma unroll 1
     for (int sl = 0; sl < 4 && ok; ++sl) {
       const int s = 4 * ch + sl;
@@ -968,21 +968,20 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
       const float tsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
       l_run = l_run * alpha + tsum;
       m_ref = m_new;
-      // the copy of P_{g-2} has read this staging buffer
-      if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sm.h.stage_free[sb], ((g - 2) >> 1) & 1,
+      // the copy of P_{g-1} has read the staging buffer
+      if (g >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.h.stage_free, (g - 1) & 1,
                                                        &sm.h.abort, p.timeout_ns))) {
         fail(sm, p.status);
         ok = false;
         continue;   // the next tile's exchange lets the row's other warp leave too
       }
-      uint8_t* const line = p_line + sb * kPBuf;
+      uint8_t* const line = p_line;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(line + ((c ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (ch == 0)
-        reinterpret_cast<float*>(sm.buf + kSSlots * kSlotBytes + sb * kPBuf + kPBytes)[row] =
-            alpha;
+        reinterpret_cast<float*>(sm.buf + kSSlots * kSlotBytes + kPBytes)[row] = alpha;
       // the copy reads the staging buffer through the async proxy
       fence_proxy_async_smem();
       __syncwarp();
@@ -1193,7 +1192,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
       mbar_init(&sm.h.s_read[i], kSmxWarps);
       mbar_init(&sm.h.s_free[i], 1);
       mbar_init(&sm.h.p_staged[i], kSmxWarps);
-      mbar_init(&sm.h.stage_free[i], 1);
       mbar_init(&sm.h.p_free[i], 1);
       mbar_init(&sm.h.p_in[i], 1);
       mbar_init(&sm.h.p_local[i], kSmxWarps);
@@ -1203,6 +1201,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     mbar_init(&sm.h.pv_done, 1);
     mbar_init(&sm.h.o_full, 1);
     mbar_init(&sm.h.o_free, kSmxWarps);
+    mbar_init(&sm.h.stage_free, 1);
     mbar_init(&sm.h.stage_full, kSmxWarps);
     mbar_init(&sm.h.v_free, 1);
     mbar_init(&sm.h.drain, 1);
