@@ -81,6 +81,9 @@ def parse():
                     help="print the oracle's CPU figure for the workload and exit (no GPU)")
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work in the CPU figure")
+    ap.add_argument("--stage-chain", type=int, choices=[0, 1], default=0,
+                    help="1: the branch call stages the cached chain's raw rows and C4 entries "
+                         "and the refresh skips them")
     ap.add_argument("--cells", type=str, default=None,
                     help="with --sweep: comma-separated cell indices (default: all 64)")
     return ap.parse_args()
@@ -428,7 +431,7 @@ def run_ours(args, world, rank, local):
               "tcgen05": _lib.TV_ATTN_TCGEN05}[args.attn_kernel]
     wl = make_workload(args.workload, rank, args.batch)
     n_sets = max(1, args.sets)
-    shape = engine.shape_for(wl, kernel)
+    shape = engine.shape_for(wl, kernel, stage_chain=args.stage_chain)
     stream = torch.cuda.current_stream()
     sets = []
     for i in range(n_sets):
@@ -436,6 +439,7 @@ def run_ours(args, world, rank, local):
             # every copy gets the same (seeded) page table, so the first copy's shape -- which
             # holds the address of its table -- serves all of them
             shape_i, st = engine.alloc_paged(wl, args.page_tokens, kernel, seed=0)
+            shape_i.stage_chain = args.stage_chain
             if i == 0:
                 shape = shape_i
         else:
@@ -648,6 +652,7 @@ def run_ours(args, world, rank, local):
                          f"{kv_bytes / 1e6:.0f} MB KV per step each",
                    "parallelism": f"replicas x{world} (requests sharded, no collective)",
                    "cuda_graph": graphs is not None,
+                   "refresh_skip": bool(args.stage_chain),
                    "kv_layout": (f"page pools, {args.page_tokens} tokens per page, pages scattered"
                                  if args.page_tokens else "contiguous per request")},
         "roofline": {"bound": "tensor", "achieved": tflops,
@@ -702,7 +707,7 @@ def run_sweep(args):
     for i in idx:
         c = cells[i]
         wl = workloads.sweep_cell(i, **c)
-        shape = engine.shape_for(wl)
+        shape = engine.shape_for(wl, stage_chain=args.stage_chain)
         st = engine.alloc_state(wl)
         rb = engine.alloc_round(wl, shape)
         engine.prefill(shape, st, rb, stream)
@@ -736,7 +741,7 @@ def run_sweep(args):
         ms = statistics.median(t_round)
         row = {"cell": i, "D": c["D"], "B": c["B"], "tree": c["kind"], "p": c["p"],
                "round_ms": ms, "attention_ms": statistics.median(t_attn),
-               "mean_accept_len": float(acc.mean()),
+               "mean_accept_len": float(acc.mean()), "refresh_skip": bool(args.stage_chain),
                "committed_tokens_per_s": float(acc.sum()) / (ms * 1e-3),
                "verified_tree_tokens_per_s": job_throughput(1, wl.B, wl.D, ms),
                "attention_kernel": "tcgen05" if _lib.tv_attn_kernel_for(shape) ==

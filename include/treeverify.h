@@ -39,7 +39,9 @@
  *   finite numbers (allocate the buffers zero-filled).
  * - Scratch pad ([TSD-V4] §4.2): scrK4/scrV4 and scrK128/scrV128 [B][D][d], one row per tree
  *   node; row v holds the compressed entry of the block that node v's token closes, or zeros.
- *   It is separate from the persistent state, which only tv_refresh_commit writes.
+ *   It is separate from the persistent state, which only tv_refresh_commit writes (with
+ *   tv_shape.stage_chain, tv_branch_compress also stages rows past the committed length, which no
+ *   call reads before tv_refresh_commit has made them part of the state).
  * - Compressor m (4 = C4, 128 = C128): block j covers positions m*j .. m*j+m-1; gate logit of
  *   token t is z_t = K_t . g_m (no scale); w = softmax(z) over the block; the entry is
  *   (sum_t w_t K_t, sum_t w_t V_t), computed in fp32 and stored in the cache dtype (round to
@@ -113,7 +115,15 @@ typedef struct tv_shape {
   int32_t page_tokens;
   int32_t max_pages;           /* logical pages per request (columns of page_table) */
   int32_t n_pool_pages;        /* pages in each pool */
-  int32_t reserved;            /* must be 0 */
+  /* Refresh skip ([TSD-V4] §4.3: the refresh can be skipped when there is a single candidate
+   * chain or the accepted chain is the latest cached one) and the two refresh schedules of §4.2
+   * (C4 promptly, C128 delayed until the accepted path is known).  0: off.  1: tv_branch_compress
+   * writes the round's cached chain -- the root, its lowest-numbered child, that node's
+   * lowest-numbered child, ... -- into the persistent raw rows L[b] + depth and the C4 entries
+   * those positions close (rows and entries past the committed length: invisible to every call
+   * until tv_refresh_commit advances L), and tv_refresh_commit copies only the accepted nodes off
+   * that chain and the accepted C128 entries.  A single-chain tree then commits by advancing L. */
+  int32_t stage_chain;
   const int32_t* page_table;   /* device [B][max_pages] int32 (page_tokens > 0 only) */
 } tv_shape;
 
@@ -172,12 +182,18 @@ int tv_prefill_compress(const tv_shape* shape, const void* rawK, const void* raw
  * sum of the m positions ending at v's position, read from the sequence prefix + path(v):
  * positions < L[b] from rawK/rawV, the others from treeK/treeV of v's ancestors.  Every other
  * row is set to zero.
- *   rawK, rawV [B][raw_cap][d] in; L [B] in; treeK, treeV [B][D][d] in (K/V of the tree tokens);
- *   parents [B][D] in; g4, g128 [d] fp32 in; scrK4, scrV4, scrK128, scrV128 [B][D][d] out
- *   (the pair of an inactive compressor is nullable).
+ * With shape->stage_chain == 1 it also stages the cached chain (see tv_shape): for every node c
+ * of that chain, rawK/rawV row L[b] + depth(c) <- treeK/treeV row c, and when c closes a C4
+ * block, C4 entry (L[b] + depth(c) + 1)/4 - 1 <- c's C4 scratch row; positions or entries past
+ * raw_cap / c4_cap are not staged.  Nothing at or below L[b] - 1 and no C128 entry is written.
+ *   rawK, rawV [B][raw_cap][d] in (and out past L[b] when staging); L [B] in; treeK, treeV
+ *   [B][D][d] in (K/V of the tree tokens); parents [B][D] in; g4, g128 [d] fp32 in;
+ *   scrK4, scrV4, scrK128, scrV128 [B][D][d] out (the pair of an inactive compressor is
+ *   nullable); c4K, c4V [B][c4_cap][d] out past L[b]/4 when staging with C4 active (else
+ *   nullable).
  * Device errors: TV_ERR_BAD_TREE, TV_ERR_CAPACITY (L > raw_cap).
  */
-int tv_branch_compress(const tv_shape* shape, const void* rawK, const void* rawV,
+int tv_branch_compress(const tv_shape* shape, void* rawK, void* rawV, void* c4K, void* c4V,
                        const int32_t* L, const void* treeK, const void* treeV,
                        const int32_t* parents, const float* g4, const float* g128, void* scrK4,
                        void* scrV4, void* scrK128, void* scrV128, int32_t* status,
@@ -257,11 +273,16 @@ int tv_accept_walk(const tv_shape* shape, const int32_t* parents, const int32_t*
  *   block, so the copy equals recompressing it); L[b] <- L + n;
  *   committed_pos[b][i] = old L + i for i < n, -1 otherwise.
  * The scratch pad must come from tv_branch_compress of the same round.
+ * With shape->stage_chain == 1 the writes tv_branch_compress already staged are skipped: the
+ * accepted nodes path[i] that are the i-th node of the cached chain (computed from parents, which
+ * must then be given) keep their staged raw row and C4 entry; every other accepted raw row and C4
+ * entry, and every C128 entry the accepted path closes, are copied as above.
+ *   parents [B][D] in (stage_chain == 1 only, else nullable)
  * Device errors: TV_ERR_CAPACITY (L+n > raw_cap or an entry beyond cap_m; request untouched),
  * TV_ERR_ARG (accept_len outside 1..D or a path id outside 0..D-1; request untouched).
  */
-int tv_refresh_commit(const tv_shape* shape, const int32_t* accept_len, const int32_t* path,
-                      const void* treeK, const void* treeV, const void* scrK4,
+int tv_refresh_commit(const tv_shape* shape, const int32_t* parents, const int32_t* accept_len,
+                      const int32_t* path, const void* treeK, const void* treeV, const void* scrK4,
                       const void* scrV4, const void* scrK128, const void* scrV128, void* rawK,
                       void* rawV, void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
                       int32_t* committed_pos, int32_t* status, tv_stream_t stream);

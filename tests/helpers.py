@@ -93,9 +93,9 @@ def to_u64(t):
     return t.detach().cpu().numpy().astype(np.int64).view(np.uint64)
 
 
-def gpu_round(wl, attn_kernel=_lib.TV_ATTN_AUTO, comp=None, commit=True):
+def gpu_round(wl, attn_kernel=_lib.TV_ATTN_AUTO, comp=None, commit=True, stage_chain=0):
     """Upload the workload, seed the compressed prefix (oracle-made unless given), run one round."""
-    shape = engine.shape_for(wl, attn_kernel)
+    shape = engine.shape_for(wl, attn_kernel, stage_chain=stage_chain)
     st = engine.alloc_state(wl)
     rb = engine.alloc_round(wl, shape)
     if comp is not None:
@@ -106,8 +106,12 @@ def gpu_round(wl, attn_kernel=_lib.TV_ATTN_AUTO, comp=None, commit=True):
     return shape, st0, st, rb
 
 
-def check_round(wl, res, st0, st, rb, requests):
-    """Compare one GPU round against the oracle results ``res`` for the listed requests."""
+def check_round(wl, res, st0, st, rb, requests, staged=False):
+    """Compare one GPU round against the oracle results ``res`` for the listed requests.
+
+    ``staged``: the round ran with tv_shape.stage_chain = 1, so raw rows at and past the new
+    length and C4 entries at and past L_new // 4 may hold staged rows of the cached chain; only
+    the state a later call can see (rows before L_new, entries before L_new // m) is compared."""
     tol = TOL[wl.dtype]
     status = int(rb.status.item())
     assert status == 0, f"device status {status}"
@@ -160,7 +164,8 @@ def check_round(wl, res, st0, st, rb, requests):
             assert np.array_equal(rows_v, r["raw_rows"][1]), f"raw V rows request {b}"
             # untouched raw rows before L and after L_new
             assert torch.equal(st.rawK[b, :L0], st0.rawK[b, :L0])
-            assert torch.equal(st.rawK[b, r["L_new"]:], st0.rawK[b, r["L_new"]:])
+            if not staged:
+                assert torch.equal(st.rawK[b, r["L_new"]:], st0.rawK[b, r["L_new"]:])
             for (m, j), (ck, cv) in r["entries"].items():
                 dk = st.c4K if m == 4 else st.c128K
                 dv = st.c4V if m == 4 else st.c128V
@@ -170,6 +175,7 @@ def check_round(wl, res, st0, st, rb, requests):
                 ck_new = st.c4K if m == 4 else st.c128K
                 ck_old = st0.c4K if m == 4 else st0.c128K
                 written = {j for (mm, j) in r["entries"] if mm == m}
-                keep = [j for j in range(ck_new.shape[1]) if j not in written]
+                end = r["L_new"] // m if (staged and m == 4) else ck_new.shape[1]
+                keep = [j for j in range(end) if j not in written]
                 assert torch.equal(ck_new[b, keep], ck_old[b, keep]), f"C{m} rows changed, request {b}"
     return errs

@@ -100,7 +100,7 @@ def test_null_pointers_rejected_before_any_launch(lib):
     rc = lib.tv_build_ancestor_mask(ctypes.byref(s), None, None, None, None, None, None, None,
                                     None, None)
     assert rc == -1 and b"null" in lib.tv_last_error_string()
-    rc = lib.tv_refresh_commit(ctypes.byref(s), *([None] * 18))
+    rc = lib.tv_refresh_commit(ctypes.byref(s), *([None] * 19))
     assert rc == -1
 
 
@@ -152,5 +152,5 @@ def test_paging_validation(lib):
     assert lib.tv_accept_walk(ctypes.byref(s), *([None] * 8)) == -2
     s = _shape(page_tokens=512, max_pages=2, n_pool_pages=8, raw_cap=1024, c4_cap=256, c128_cap=8)
     assert lib.tv_accept_walk(ctypes.byref(s), *([None] * 8)) == -1      # page_table is null
-    s.reserved = 1
+    s.stage_chain = 2
     assert lib.tv_workspace_size(ctypes.byref(s)) == 0

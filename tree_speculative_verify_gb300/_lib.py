@@ -43,7 +43,7 @@ class tv_shape(ctypes.Structure):
         ("attn_kernel", ctypes.c_int32), ("raw_cap", ctypes.c_int64), ("c4_cap", ctypes.c_int64),
         ("c128_cap", ctypes.c_int64), ("page_tokens", ctypes.c_int32),
         ("max_pages", ctypes.c_int32), ("n_pool_pages", ctypes.c_int32),
-        ("reserved", ctypes.c_int32), ("page_table", ctypes.c_void_p),
+        ("stage_chain", ctypes.c_int32), ("page_table", ctypes.c_void_p),
     ]
 
 
@@ -66,13 +66,13 @@ _SIGS = {
     "tv_attn_kernel_for": ([_SHAPE], ctypes.c_int),
     "tv_build_ancestor_mask": ([_SHAPE] + [_P] * 8 + [_P], ctypes.c_int),
     "tv_prefill_compress": ([_SHAPE] + [_P] * 10 + [_P], ctypes.c_int),
-    "tv_branch_compress": ([_SHAPE] + [_P] * 13 + [_P], ctypes.c_int),
+    "tv_branch_compress": ([_SHAPE] + [_P] * 15 + [_P], ctypes.c_int),
     "tv_tree_verify_attn": ([_SHAPE] + [_P] * 19 + [ctypes.c_float, _P, _P, _P, ctypes.c_size_t,
                                                     _P, _P], ctypes.c_int),
     "tv_tree_verify_attn_noalloc": ([_SHAPE] + [_P] * 19 + [ctypes.c_float, _P, _P, _P, _P],
                                     ctypes.c_int),
     "tv_accept_walk": ([_SHAPE] + [_P] * 7 + [_P], ctypes.c_int),
-    "tv_refresh_commit": ([_SHAPE] + [_P] * 17 + [_P], ctypes.c_int),
+    "tv_refresh_commit": ([_SHAPE] + [_P] * 18 + [_P], ctypes.c_int),
     "tv_indexer_workspace_size": ([_SHAPE], ctypes.c_size_t),
     "tv_indexer_topk": ([_SHAPE, ctypes.c_int] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
                         ctypes.c_int),
@@ -104,12 +104,14 @@ def version():
 
 def make_shape(*, B, D, H, d, W=0, tail_mode=TV_TAIL_WINDOW, comp_mask=TV_COMP_C4 | TV_COMP_C128,
                dtype=TV_BF16, n_sel=0, attn_kernel=TV_ATTN_AUTO, raw_cap=0, c4_cap=0, c128_cap=0,
-               page_tokens=0, max_pages=0, n_pool_pages=0, page_table=None):
+               page_tokens=0, max_pages=0, n_pool_pages=0, page_table=None, stage_chain=0):
     """``page_table``: a CUDA int32 tensor [B][max_pages] (paged pools only); the shape keeps its
-    device address, so the tensor must outlive the shape's use."""
+    device address, so the tensor must outlive the shape's use.  ``stage_chain``: 1 stages the
+    cached chain's raw rows and C4 entries in tv_branch_compress and skips them in
+    tv_refresh_commit."""
     pt = None if page_table is None else _p(page_table).value
     return tv_shape(B, D, H, d, W, tail_mode, comp_mask, dtype, n_sel, attn_kernel, raw_cap,
-                    c4_cap, c128_cap, page_tokens, max_pages, n_pool_pages, 0, pt)
+                    c4_cap, c128_cap, page_tokens, max_pages, n_pool_pages, stage_chain, pt)
 
 
 def _p(t):
@@ -163,11 +165,12 @@ def tv_prefill_compress(shape, rawK, rawV, L, g4, g128, c4K, c4V, c128K, c128V, 
     _check("tv_prefill_compress", rc)
 
 
-def tv_branch_compress(shape, rawK, rawV, L, treeK, treeV, parents, g4, g128, scrK4, scrV4,
-                       scrK128, scrV128, status, stream=None):
-    rc = load().tv_branch_compress(ctypes.byref(shape), _p(rawK), _p(rawV), _p(L), _p(treeK),
-                                   _p(treeV), _p(parents), _p(g4), _p(g128), _p(scrK4), _p(scrV4),
-                                   _p(scrK128), _p(scrV128), _p(status), _stream(stream))
+def tv_branch_compress(shape, rawK, rawV, c4K, c4V, L, treeK, treeV, parents, g4, g128, scrK4,
+                       scrV4, scrK128, scrV128, status, stream=None):
+    rc = load().tv_branch_compress(ctypes.byref(shape), _p(rawK), _p(rawV), _p(c4K), _p(c4V),
+                                   _p(L), _p(treeK), _p(treeV), _p(parents), _p(g4), _p(g128),
+                                   _p(scrK4), _p(scrV4), _p(scrK128), _p(scrV128), _p(status),
+                                   _stream(stream))
     _check("tv_branch_compress", rc)
 
 
@@ -203,12 +206,13 @@ def tv_accept_walk(shape, parents, draft, target, accept_len, path, bonus, statu
     _check("tv_accept_walk", rc)
 
 
-def tv_refresh_commit(shape, accept_len, path, treeK, treeV, scrK4, scrV4, scrK128, scrV128, rawK,
-                      rawV, c4K, c4V, c128K, c128V, L, committed_pos, status, stream=None):
-    rc = load().tv_refresh_commit(ctypes.byref(shape), _p(accept_len), _p(path), _p(treeK),
-                                  _p(treeV), _p(scrK4), _p(scrV4), _p(scrK128), _p(scrV128),
-                                  _p(rawK), _p(rawV), _p(c4K), _p(c4V), _p(c128K), _p(c128V),
-                                  _p(L), _p(committed_pos), _p(status), _stream(stream))
+def tv_refresh_commit(shape, parents, accept_len, path, treeK, treeV, scrK4, scrV4, scrK128,
+                      scrV128, rawK, rawV, c4K, c4V, c128K, c128V, L, committed_pos, status,
+                      stream=None):
+    rc = load().tv_refresh_commit(ctypes.byref(shape), _p(parents), _p(accept_len), _p(path),
+                                  _p(treeK), _p(treeV), _p(scrK4), _p(scrV4), _p(scrK128),
+                                  _p(scrV128), _p(rawK), _p(rawV), _p(c4K), _p(c4V), _p(c128K),
+                                  _p(c128V), _p(L), _p(committed_pos), _p(status), _stream(stream))
     _check("tv_refresh_commit", rc)
 
 

@@ -77,7 +77,8 @@ static int check_shape(const tv_shape* s, const char* fn) {
     return tv_set_error(TV_ERR_SHAPE, "%s: capacities must be in 0..2^30", fn);
   if ((int64_t)s->B * s->D * s->H > ((int64_t)1 << 31) / 1024)
     return tv_set_error(TV_ERR_SHAPE, "%s: B*D*H too large", fn);
-  if (s->reserved != 0) return tv_set_error(TV_ERR_ARG, "%s: reserved field must be 0", fn);
+  if (s->stage_chain != 0 && s->stage_chain != 1)
+    return tv_set_error(TV_ERR_ARG, "%s: stage_chain must be 0 or 1", fn);
   if (s->page_tokens != 0) {
     const int64_t P = s->page_tokens, G = s->max_pages;
     if (P < 0 || P % 512 != 0 || P > (1 << 20))
@@ -110,14 +111,16 @@ int tv_launch_plan(const tv_shape* s, const int32_t* parents, const int32_t* L, 
 int tv_launch_prefill(const tv_shape* s, const void* rawK, const void* rawV, const int32_t* L,
                       const float* g4, const float* g128, void* c4K, void* c4V, void* c128K,
                       void* c128V, int32_t* status, cudaStream_t stream);
-int tv_launch_branch(const tv_shape* s, const void* rawK, const void* rawV, const int32_t* L,
+int tv_launch_branch(const tv_shape* s, void* rawK, void* rawV, void* c4K, void* c4V,
+                     const int32_t* L,
                      const void* treeK, const void* treeV, const int32_t* parents,
                      const float* g4, const float* g128, void* scrK4, void* scrV4,
                      void* scrK128, void* scrV128, int32_t* status, cudaStream_t stream);
 int tv_launch_accept(const tv_shape* s, const int32_t* parents, const int32_t* draft,
                      const int32_t* target, int32_t* accept_len, int32_t* path, int32_t* bonus,
                      int32_t* status, cudaStream_t stream);
-int tv_launch_refresh(const tv_shape* s, const int32_t* accept_len, const int32_t* path,
+int tv_launch_refresh(const tv_shape* s, const int32_t* parents, const int32_t* accept_len,
+                      const int32_t* path,
                       const void* treeK, const void* treeV, const void* scrK4, const void* scrV4,
                       const void* scrK128, const void* scrV128, void* rawK, void* rawV,
                       void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
@@ -233,7 +236,7 @@ extern "C" int tv_prefill_compress(const tv_shape* s, const void* rawK, const vo
                            (cudaStream_t)stream);
 }
 
-extern "C" int tv_branch_compress(const tv_shape* s, const void* rawK, const void* rawV,
+extern "C" int tv_branch_compress(const tv_shape* s, void* rawK, void* rawV, void* c4K, void* c4V,
                                   const int32_t* L, const void* treeK, const void* treeV,
                                   const int32_t* parents, const float* g4, const float* g128,
                                   void* scrK4, void* scrV4, void* scrK128, void* scrV128,
@@ -258,8 +261,12 @@ extern "C" int tv_branch_compress(const tv_shape* s, const void* rawK, const voi
     TV_REQUIRE(scrK128, fn);
     TV_REQUIRE(scrV128, fn);
   }
-  return tv_launch_branch(s, rawK, rawV, L, treeK, treeV, parents, g4, g128, scrK4, scrV4,
-                          scrK128, scrV128, status, (cudaStream_t)stream);
+  if (s->stage_chain && has_c4(s)) {
+    TV_REQUIRE(c4K, fn);
+    TV_REQUIRE(c4V, fn);
+  }
+  return tv_launch_branch(s, rawK, rawV, c4K, c4V, L, treeK, treeV, parents, g4, g128, scrK4,
+                          scrV4, scrK128, scrV128, status, (cudaStream_t)stream);
 }
 
 template <typename T>
@@ -410,8 +417,9 @@ extern "C" int tv_accept_walk(const tv_shape* s, const int32_t* parents, const i
                           (cudaStream_t)stream);
 }
 
-extern "C" int tv_refresh_commit(const tv_shape* s, const int32_t* accept_len,
-                                 const int32_t* path, const void* treeK, const void* treeV,
+extern "C" int tv_refresh_commit(const tv_shape* s, const int32_t* parents,
+                                 const int32_t* accept_len, const int32_t* path,
+                                 const void* treeK, const void* treeV,
                                  const void* scrK4, const void* scrV4, const void* scrK128,
                                  const void* scrV128, void* rawK, void* rawV, void* c4K,
                                  void* c4V, void* c128K, void* c128V, int32_t* L,
@@ -428,6 +436,7 @@ extern "C" int tv_refresh_commit(const tv_shape* s, const int32_t* accept_len,
   TV_REQUIRE(L, fn);
   TV_REQUIRE(committed_pos, fn);
   TV_REQUIRE(status, fn);
+  if (s->stage_chain) TV_REQUIRE(parents, fn);
   if (has_c4(s)) {
     TV_REQUIRE(scrK4, fn);
     TV_REQUIRE(scrV4, fn);
@@ -440,8 +449,8 @@ extern "C" int tv_refresh_commit(const tv_shape* s, const int32_t* accept_len,
     TV_REQUIRE(c128K, fn);
     TV_REQUIRE(c128V, fn);
   }
-  return tv_launch_refresh(s, accept_len, path, treeK, treeV, scrK4, scrV4, scrK128, scrV128,
-                           rawK, rawV, c4K, c4V, c128K, c128V, L, committed_pos, status,
+  return tv_launch_refresh(s, parents, accept_len, path, treeK, treeV, scrK4, scrV4, scrK128,
+                           scrV128, rawK, rawV, c4K, c4V, c128K, c128V, L, committed_pos, status,
                            (cudaStream_t)stream);
 }
 

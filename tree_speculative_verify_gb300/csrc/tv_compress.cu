@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) prefill_kernel(Paging pg,
 // with zeros.
 template <typename T>
 __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(Paging pg, int D, int d, int comp_mask, int64_t raw_cap,
-                              const T* __restrict__ rawK, const T* __restrict__ rawV,
+                              T* rawK, T* rawV, int stage, int64_t c4_cap, T* c4K, T* c4V,
                               const int32_t* __restrict__ L, const T* __restrict__ treeK,
                               const T* __restrict__ treeV, const int32_t* __restrict__ parents,
                               const float* __restrict__ g4, const float* __restrict__ g128,
@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(Paging pg, 
   __shared__ int s_par[kMaxD];
   __shared__ int s_depth;
   __shared__ int s_ok;
+  __shared__ int s_cached;   // v lies on the round's cached chain
   const int v = blockIdx.x;
   const int b = blockIdx.y;
   int which = blockIdx.z;  // index among active compressors
@@ -287,17 +288,38 @@ __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(Paging pg, 
       ++dep;
     }
     if (ok && s_par[0] != -1) ok = 0;
+    int cached = 0;
     if (ok) {
       for (int k = 0; k <= dep; ++k) path[k] = chain[dep - k];
+      // cached chain: every step goes to the lowest-numbered child of the previous node
+      cached = 1;
+      for (int k = 0; k < dep && cached; ++k)
+        for (int u = 1; u < path[k + 1]; ++u)
+          if (s_par[u] == path[k]) {
+            cached = 0;
+            break;
+          }
     } else {
       record_error(status, (Lb < 0 || Lb > raw_cap) ? TV_ERR_CAPACITY : TV_ERR_BAD_TREE);
     }
     s_depth = dep;
     s_ok = ok;
+    s_cached = cached;
   }
   __syncthreads();
   const int pos = Lb + s_depth;
   const bool closes = s_ok && ((pos + 1) % m == 0);
+  // staging (refresh skip): the cached chain's raw row goes to its final place past L now, once
+  // per node (by the CTA of the first active compressor)
+  const bool stage_here = stage && s_ok && s_cached;
+  if (stage_here && which == 0 && pos < raw_cap) {
+    const int64_t dst = layer_row(pg, b, pos, raw_cap, 1, status) * d;
+    const int64_t src = ((int64_t)b * D + v) * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+      rawK[dst + i] = treeK[src + i];
+      rawV[dst + i] = treeV[src + i];
+    }
+  }
   if (!closes) {
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
       store_f(outK + out + i, 0.f);
@@ -319,6 +341,17 @@ __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(Paging pg, 
   }
   __syncthreads();
   gated_block_sum<T>(rowK, rowV, m, d, g, outK + out, outV + out, w, red);
+  // C4 refreshes promptly: a cached-chain node's C4 entry is also staged in its final place
+  // (C128 entries wait for the accepted path)
+  const int64_t entry = (pos + 1) / 4 - 1;
+  if (stage_here && m == 4 && entry < c4_cap) {
+    __syncthreads();   // the entry this CTA just wrote is visible to all its threads
+    const int64_t dst = layer_row(pg, b, entry, c4_cap, 4, status) * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+      c4K[dst + i] = outK[out + i];
+      c4V[dst + i] = outV[out + i];
+    }
+  }
 }
 
 // ---- refresh: commit the accepted path --------------------------------------------------------
@@ -326,7 +359,8 @@ __global__ void __launch_bounds__(kCompressThreads, 2) branch_kernel(Paging pg, 
 // scratch rows of accepted nodes that close a block into the persistent entries (all rows in
 // parallel: each 16-byte chunk of each row is one thread's job), then advances L.
 __global__ void refresh_kernel(Paging pg, int D, int d, int es, int comp_mask, int64_t raw_cap,
-                               int64_t c4_cap, int64_t c128_cap,
+                               int64_t c4_cap, int64_t c128_cap, int stage,
+                               const int32_t* __restrict__ parents,
                                const int32_t* __restrict__ accept_len,
                                const int32_t* __restrict__ path_all, const char* treeK,
                                const char* treeV, const char* scrK4, const char* scrV4,
@@ -359,18 +393,40 @@ __global__ void refresh_kernel(Paging pg, int D, int d, int es, int comp_mask, i
       if ((comp_mask & TV_COMP_C128) && Lnew / 128 > c128_cap) { ok = 0; code = TV_ERR_CAPACITY; }
     }
     if (!ok) record_error(status, code);
+    // with staging, the accepted nodes on the cached chain (the root, its lowest-numbered child,
+    // ...) already sit in their final raw rows and C4 entries: the accepted path follows that
+    // chain up to the first node where it leaves it
+    int staged = 0;
+    if (ok && stage) {
+      const int32_t* par = parents + (int64_t)b * D;
+      int c = 0;
+      while (staged < n && path[staged] == c) {
+        ++staged;
+        int next = -1;
+        for (int u = c + 1; u < D; ++u)
+          if (par[u] == c) {
+            next = u;
+            break;
+          }
+        if (next < 0) break;
+        c = next;
+      }
+    }
     int jobs = 0;
     if (ok) {
       for (int i = 0; i < n; ++i) {
         const int64_t src = ((int64_t)b * D + path[i]) * row_bytes;
-        const int64_t dst = layer_row(pg, b, Lb + i, raw_cap, 1, status) * row_bytes;
-        s_srcK[jobs] = treeK + src;
-        s_srcV[jobs] = treeV + src;
-        s_dstK[jobs] = rawK + dst;
-        s_dstV[jobs] = rawV + dst;
-        ++jobs;
+        const bool on_chain = i < staged;
+        if (!on_chain) {
+          const int64_t dst = layer_row(pg, b, Lb + i, raw_cap, 1, status) * row_bytes;
+          s_srcK[jobs] = treeK + src;
+          s_srcV[jobs] = treeV + src;
+          s_dstK[jobs] = rawK + dst;
+          s_dstV[jobs] = rawV + dst;
+          ++jobs;
+        }
         const int e = Lb + i;
-        if ((comp_mask & TV_COMP_C4) && ((e + 1) & 3) == 0) {
+        if ((comp_mask & TV_COMP_C4) && ((e + 1) & 3) == 0 && !on_chain) {
           const int64_t cd = layer_row(pg, b, (e + 1) / 4 - 1, c4_cap, 4, status) * row_bytes;
           s_srcK[jobs] = scrK4 + src;
           s_srcV[jobs] = scrV4 + src;
@@ -448,7 +504,7 @@ int tv_launch_prefill(const tv_shape* s, const void* rawK, const void* rawV, con
                                  stream);
 }
 
-int tv_launch_branch(const tv_shape* s, const void* rawK, const void* rawV, const int32_t* L,
+int tv_launch_branch(const tv_shape* s, void* rawK, void* rawV, void* c4K, void* c4V, const int32_t* L,
                      const void* treeK, const void* treeV, const int32_t* parents,
                      const float* g4, const float* g128, void* scrK4, void* scrV4,
                      void* scrK128, void* scrV128, int32_t* status, cudaStream_t stream) {
@@ -457,27 +513,31 @@ int tv_launch_branch(const tv_shape* s, const void* rawK, const void* rawV, cons
   if (s->dtype == TV_BF16) {
     using T = __nv_bfloat16;
     tv::branch_kernel<T><<<grid, tv::kCompressThreads, 0, stream>>>(
-        tv::paging_of(s), s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
+        tv::paging_of(s), s->D, s->d, s->comp_mask, s->raw_cap, (T*)rawK, (T*)rawV,
+        s->stage_chain, s->c4_cap, (T*)c4K, (T*)c4V, L,
         (const T*)treeK, (const T*)treeV, parents, g4, g128, (T*)scrK4, (T*)scrV4,
         (T*)scrK128, (T*)scrV128, status);
   } else {
     using T = float;
     tv::branch_kernel<T><<<grid, tv::kCompressThreads, 0, stream>>>(
-        tv::paging_of(s), s->D, s->d, s->comp_mask, s->raw_cap, (const T*)rawK, (const T*)rawV, L,
+        tv::paging_of(s), s->D, s->d, s->comp_mask, s->raw_cap, (T*)rawK, (T*)rawV,
+        s->stage_chain, s->c4_cap, (T*)c4K, (T*)c4V, L,
         (const T*)treeK, (const T*)treeV, parents, g4, g128, (T*)scrK4, (T*)scrV4,
         (T*)scrK128, (T*)scrV128, status);
   }
   return tv_check_launch("tv_branch_compress");
 }
 
-int tv_launch_refresh(const tv_shape* s, const int32_t* accept_len, const int32_t* path,
+int tv_launch_refresh(const tv_shape* s, const int32_t* parents, const int32_t* accept_len,
+                      const int32_t* path,
                       const void* treeK, const void* treeV, const void* scrK4, const void* scrV4,
                       const void* scrK128, const void* scrV128, void* rawK, void* rawV,
                       void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
                       int32_t* committed, int32_t* status, cudaStream_t stream) {
   const int es = s->dtype == TV_BF16 ? 2 : 4;
   tv::refresh_kernel<<<s->B, 256, 0, stream>>>(
-      tv::paging_of(s), s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap, accept_len, path,
+      tv::paging_of(s), s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap,
+      s->stage_chain, parents, accept_len, path,
       (const char*)treeK, (const char*)treeV, (const char*)scrK4, (const char*)scrV4,
       (const char*)scrK128, (const char*)scrV128, (char*)rawK, (char*)rawV, (char*)c4K,
       (char*)c4V, (char*)c128K, (char*)c128V, L, committed, status);

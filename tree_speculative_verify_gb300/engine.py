@@ -17,7 +17,7 @@ import torch
 from . import _lib
 
 
-def shape_for(wl, attn_kernel=_lib.TV_ATTN_AUTO, B=None):
+def shape_for(wl, attn_kernel=_lib.TV_ATTN_AUTO, B=None, stage_chain=0):
     comp = 0
     if 4 in wl.ms:
         comp |= _lib.TV_COMP_C4
@@ -28,7 +28,8 @@ def shape_for(wl, attn_kernel=_lib.TV_ATTN_AUTO, B=None):
         tail_mode=_lib.TV_TAIL_WINDOW if wl.tail_mode == "window" else _lib.TV_TAIL_REMAINDER,
         comp_mask=comp, dtype=_lib.TV_F32 if wl.dtype == "f32" else _lib.TV_BF16,
         n_sel=wl.n_sel, attn_kernel=attn_kernel, raw_cap=wl.raw_cap,
-        c4_cap=wl.cap4 if 4 in wl.ms else 0, c128_cap=wl.cap128 if 128 in wl.ms else 0)
+        c4_cap=wl.cap4 if 4 in wl.ms else 0, c128_cap=wl.cap128 if 128 in wl.ms else 0,
+        stage_chain=stage_chain)
 
 
 @dataclass
@@ -181,8 +182,9 @@ def plan(shape, st, rb, stream=None):
 
 
 def branch_compress(shape, st, rb, stream=None):
-    _lib.tv_branch_compress(shape, st.rawK, st.rawV, st.L, rb.treeK, rb.treeV, rb.parents, rb.g4,
-                            rb.g128, rb.scrK4, rb.scrV4, rb.scrK128, rb.scrV128, rb.status, stream)
+    _lib.tv_branch_compress(shape, st.rawK, st.rawV, st.c4K, st.c4V, st.L, rb.treeK, rb.treeV,
+                            rb.parents, rb.g4, rb.g128, rb.scrK4, rb.scrV4, rb.scrK128, rb.scrV128,
+                            rb.status, stream)
 
 
 def attention(shape, st, rb, scale=None, stream=None):
@@ -200,9 +202,9 @@ def accept(shape, st, rb, stream=None):
 
 
 def refresh(shape, st, rb, stream=None):
-    _lib.tv_refresh_commit(shape, rb.accept_len, rb.path, rb.treeK, rb.treeV, rb.scrK4, rb.scrV4,
-                           rb.scrK128, rb.scrV128, st.rawK, st.rawV, st.c4K, st.c4V, st.c128K,
-                           st.c128V, st.L, rb.committed, rb.status, stream)
+    _lib.tv_refresh_commit(shape, rb.parents, rb.accept_len, rb.path, rb.treeK, rb.treeV,
+                           rb.scrK4, rb.scrV4, rb.scrK128, rb.scrV128, st.rawK, st.rawV, st.c4K,
+                           st.c4V, st.c128K, st.c128V, st.L, rb.committed, rb.status, stream)
 
 
 def verify_round(shape, st, rb, scale=None, stream=None, commit=True, select=False):
