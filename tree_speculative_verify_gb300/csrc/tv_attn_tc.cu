@@ -165,6 +165,10 @@ __device__ __forceinline__ Tile tile_of(const Layout& y, int t) {
 // requests first, so the last wave holds the shortest work items.  rank(b) = number of requests
 // with more tiles, ties broken by index; order[rank(b)] = b.
 __global__ void order_kernel(Params p, int32_t* order) {
+  // a programmatic dependent of the scratch-pad kernel: waits for it, then lets the attention
+  // kernel start its prologue
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int tiles[];   // B tile counts
   for (int j = threadIdx.x; j < p.B; j += blockDim.x) tiles[j] = layout_of(p, j).T;
   __syncthreads();
@@ -1170,9 +1174,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   // the swizzled operand tiles need 1 KB alignment; the dynamic window starts 1 KB aligned
   if ((smem_u32(smem_raw) & 1023u) != 0) {
+    pdl_wait();
     if (threadIdx.x == 0) record_error(p.status, TV_ERR_CUDA);
     return;
   }
+  pdl_launch_dependents();   // the acceptance walk reads nothing this kernel writes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // clusters of 4 consecutive CTAs; rank = 2 * (0: pair S, 1: pair O) + (row tile & 1)
   const uint32_t rank = blockIdx.x & 3;
@@ -1219,6 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   tc_fence_before();
   cluster_sync();   // every CTA's barriers exist before any remote arrive, store or pair MMA
   tc_fence_after();
+  // launched as a programmatic dependent of the scheduling kernel: the set-up above overlaps it;
+  // every read of the round's inputs comes after it has completed
+  pdl_wait();
 
   if (warp == 0) {
     producer<kPaged>(p, sm, role_s, sub);
@@ -1545,7 +1554,9 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
     if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 paged gather)")) return rc;
   }
   // one CTA ranks all requests (B <= 12288 fits its default shared memory)
-  order_kernel<<<1, 1024, (size_t)s->B * sizeof(int), stream>>>(p, order);
+  if (tv::launch_pdl(order_kernel, dim3(1), dim3(1024), (size_t)s->B * sizeof(int), stream, p,
+                 order) != cudaSuccess)
+    return tv_check_launch("tv_tree_verify_attn (tcgen05 schedule launch)");
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;
   if (cluster_slots() <= 0)
     return tv_check_launch("tv_tree_verify_attn (tcgen05 kernel attributes)");
@@ -1559,13 +1570,15 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kClusterCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // after the schedule
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t le = paged ? cudaLaunchKernelEx(&cfg, attn_kernel<true>, p)
                                : cudaLaunchKernelEx(&cfg, attn_kernel<false>, p);
   if (le != cudaSuccess)

@@ -42,6 +42,34 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the kernel
+// before it in the stream still runs, once every CTA of that kernel has called
+// pdl_launch_dependents (or finished).  It must call pdl_wait before it reads anything that
+// kernel writes and before it writes anything that kernel reads, and before it exits, so that
+// its own completion still implies the completion of everything before it in the stream.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the kernel this one depends on programmatically has completed and its memory
+// operations are visible (returns at once for a kernel launched without such a dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Lowest raw position visible from a query at position p.
 __device__ __forceinline__ int raw_lo_of(int p, int tail_mode, int W, int m_min) {
   if (tail_mode == TV_TAIL_WINDOW) return p - W > 0 ? p - W : 0;

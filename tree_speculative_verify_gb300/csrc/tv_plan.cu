@@ -14,12 +14,17 @@ __global__ void plan_kernel(int B, int D, int W, int tail_mode, int comp_mask,
                             uint64_t* __restrict__ anc, int32_t* __restrict__ depth,
                             int32_t* __restrict__ raw_lo, uint64_t* __restrict__ scr_vis4,
                             uint64_t* __restrict__ scr_vis128, int32_t* status) {
+  pdl_launch_dependents();   // the scratch-pad kernel reads nothing this one writes
   const int warps_per_block = blockDim.x / 32;
   const int b = blockIdx.x * warps_per_block + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (b >= B) return;
-  const int32_t* par = parents + (int64_t)b * D;
+  // the request's parents in shared memory (warp-private), so the walks below cost no round trips
+  __shared__ int s_par[4][kMaxD];
+  int* par = s_par[(threadIdx.x / 32) & 3];
   const int Lb = L[b];
+  for (int v = lane; v < D; v += 32) par[v] = parents[(int64_t)b * D + v];
+  __syncwarp();
 
   // validate the tree: every node must name an earlier node (root: -1)
   bool ok = Lb >= 0;
