@@ -75,6 +75,8 @@ typedef struct CUstream_st* tv_stream_t; /* the same handle type as cudaStream_t
 #define TV_ERR_WORKSPACE (-7)  /* workspace too small (see tv_workspace_size) */
 #define TV_ERR_TIMEOUT (-8)    /* a bounded device-side wait ran out (kernel returned early) */
 #define TV_ERR_SELECTION (-9)  /* a selection index is outside the request's C4 entries */
+#define TV_ERR_BOUNDS (-10)    /* bounds-checked build only: a global index failed its range
+                                  check (the access was skipped; the site is printed once) */
 
 /* tv_shape.tail_mode */
 #define TV_TAIL_WINDOW 0
@@ -233,12 +235,16 @@ int tv_tree_verify_attn(const tv_shape* shape, const void* Q, const void* c4K, c
  * not pay cudaMalloc's implicit synchronisation, a plug-in host without an allocator).  The report
  * has no counterpart: this is a convenience of the library.  Same arguments, semantics and
  * outputs as tv_tree_verify_attn, minus workspace / ws_bytes.  The split-KV partial results live
- * in a 32 MiB array inside the library image, held by every GPU that loads the library until the
- * process exits; a shape whose tv_workspace_size exceeds it is rejected with TV_ERR_WORKSPACE.
- * The first call on a device resolves the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  All calls share the array:
- * calls that overlap on the GPU race on it (its previous contents are never read, nothing needs
- * clearing).  It allocates nothing, neither on the device nor through any library.
+ * in a 32 MiB array inside the library image, held by every GPU that loads the library's device
+ * code until the process exits; a shape whose tv_workspace_size exceeds it is rejected with
+ * TV_ERR_WORKSPACE.  Under CUDA's lazy module loading (the default) the device code, and with it
+ * the 32 MiB, is loaded on a device at the first call there that resolves the array: call
+ * tv_noalloc_prepare once per device at start-up, before reserving a memory pool and before any
+ * stream capture; later calls take no device memory.  The array's address is looked up in the
+ * caller's current context on every call.  All calls share the array: calls that overlap on the
+ * GPU race on it (its previous contents are never read, nothing needs clearing).  Host errors name
+ * tv_tree_verify_attn_noalloc.  It allocates nothing, neither on the device nor through any
+ * library.
  */
 int tv_tree_verify_attn_noalloc(const tv_shape* shape, const void* Q, const void* c4K,
                                 const void* c4V, const int32_t* sel, const void* c128K,
@@ -249,6 +255,14 @@ int tv_tree_verify_attn_noalloc(const tv_shape* shape, const void* Q, const void
                                 const void* scrK4, const void* scrV4, const void* scrK128,
                                 const void* scrV128, float scale, void* O, float* lse,
                                 int32_t* status, tv_stream_t stream);
+
+/*
+ * Loads the library's device code on the current device, with the built-in scratch of
+ * tv_tree_verify_attn_noalloc (32 MiB), so that later calls take no device memory.  Call it once
+ * per device before handing the free memory to a pool.  Returns TV_OK, or TV_ERR_CUDA if the
+ * device code cannot be loaded (for instance when less than 32 MiB is free).
+ */
+int tv_noalloc_prepare(void);
 
 /*
  * Accepted-path selection ([TSD-V4] §3.2, §4.1): greedy walk from the root; at each node take

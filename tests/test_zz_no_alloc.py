@@ -80,3 +80,33 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
         _lib.tv_tree_verify_attn_noalloc(shape, *([dummy] * 19), 0.05, dummy, dummy,
                                          torch.zeros(1, dtype=torch.int32, device="cuda"))
     assert e.value.code == -7
+
+
+def test_prepare_then_calls_take_no_device_memory():
+    """After tv_noalloc_prepare, the entry point takes no device memory: the free memory the
+    driver reports is the same before and after several calls."""
+    _lib.tv_noalloc_prepare()
+    wl = workloads.small()
+    shape, st, rb = _prepared(wl)
+    O = torch.empty_like(rb.O)
+    lse = torch.empty_like(rb.lse)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc(shape, st, rb, O, lse)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert int(rb.status.item()) == 0
+    assert free1 == free0, (free0, free1)
+
+
+def test_host_errors_name_the_noalloc_entry_point():
+    wl = workloads.small()
+    shape, st, rb = _prepared(wl)
+    with pytest.raises(_lib.TreeVerifyError) as e:
+        _lib.tv_tree_verify_attn_noalloc(
+            shape, rb.Q, st.c4K, st.c4V, rb.sel, st.c128K, st.c128V, st.rawK, st.rawV, st.L,
+            rb.treeK, rb.treeV, rb.anc, rb.raw_lo, rb.vis4, rb.vis128, rb.scrK4, rb.scrV4,
+            rb.scrK128, rb.scrV128, -1.0, rb.O, rb.lse, rb.status)
+    # the library's own message (not the binding's prefix) names the entry point
+    assert _lib.load().tv_last_error_string().decode().startswith("tv_tree_verify_attn_noalloc")

@@ -13,13 +13,15 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtreeverify.so")
+# TV_LIB_CHECKED=1 loads the bounds-checked debug build of the same library instead
+LIB_PATH = os.path.join(_PKG, "libtreeverify_checked.so" if os.environ.get("TV_LIB_CHECKED") == "1"
+                        else "libtreeverify.so")
 
 TV_OK = 0
 TV_ERR = {
     -1: "TV_ERR_ARG", -2: "TV_ERR_SHAPE", -3: "TV_ERR_BAD_TREE", -4: "TV_ERR_CAPACITY",
     -5: "TV_ERR_DTYPE", -6: "TV_ERR_CUDA", -7: "TV_ERR_WORKSPACE", -8: "TV_ERR_TIMEOUT",
-    -9: "TV_ERR_SELECTION",
+    -9: "TV_ERR_SELECTION", -10: "TV_ERR_BOUNDS",
 }
 TV_TAIL_WINDOW, TV_TAIL_REMAINDER = 0, 1
 TV_COMP_C4, TV_COMP_C128 = 1, 2
@@ -31,7 +33,7 @@ EXPORTS = (
     "tv_attn_kernel_for",
     "tv_build_ancestor_mask", "tv_prefill_compress", "tv_branch_compress",
     "tv_tree_verify_attn", "tv_accept_walk", "tv_refresh_commit", "tv_tree_verify_attn_noalloc",
-    "tv_indexer_workspace_size", "tv_indexer_topk", "tv_debug_attn_timeout",
+    "tv_indexer_workspace_size", "tv_indexer_topk", "tv_debug_attn_timeout", "tv_noalloc_prepare",
 )
 
 
@@ -76,6 +78,7 @@ _SIGS = {
     "tv_indexer_workspace_size": ([_SHAPE], ctypes.c_size_t),
     "tv_indexer_topk": ([_SHAPE, ctypes.c_int] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
                         ctypes.c_int),
+    "tv_noalloc_prepare": ([], ctypes.c_int),
     "tv_debug_attn_timeout": ([ctypes.c_int64, ctypes.c_int32], ctypes.c_int),
 }
 
@@ -214,6 +217,11 @@ def tv_refresh_commit(shape, parents, accept_len, path, treeK, treeV, scrK4, scr
                                   _p(scrV128), _p(rawK), _p(rawV), _p(c4K), _p(c4V), _p(c128K),
                                   _p(c128V), _p(L), _p(committed_pos), _p(status), _stream(stream))
     _check("tv_refresh_commit", rc)
+
+
+def tv_noalloc_prepare():
+    """Load the library's device code (with the 32 MiB built-in scratch) on the current device."""
+    _check("tv_noalloc_prepare", load().tv_noalloc_prepare())
 
 
 def tv_indexer_workspace_size(shape):

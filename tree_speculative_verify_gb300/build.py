@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtreeverify.so")
+# the bounds-checked debug build (-DTV_CHECK_BOUNDS): every checked global index that fails its
+# range check records TV_ERR_BOUNDS and skips the access (see tv_common.cuh)
+LIB_CHECKED = os.path.join(PKG, "libtreeverify_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -43,24 +46,28 @@ def _inputs():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB
+def build(force=False, verbose=False, extra_flags=(), checked=False):
+    """Compile and link the library (checked: the bounds-checked debug build, a separate file);
+    returns its path."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
+    objdir = os.path.join(BUILD, "checked") if checked else BUILD
+    os.makedirs(objdir, exist_ok=True)
     srcs = _sources()
+    flags = list(extra_flags) + (["-DTV_CHECK_BOUNDS"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        obj = os.path.join(objdir, os.path.basename(src).replace(".cu", ".o"))
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -71,17 +78,18 @@ def build(force=False, verbose=False, extra_flags=()):
     workers = min(len(srcs), os.cpu_count() or 4)
     with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     force = "--force" in sys.argv
     verbose = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []
-    print(build(force=force or bool(extra), verbose=verbose or bool(extra), extra_flags=extra))
+    print(build(force=force or bool(extra), verbose=verbose or bool(extra), extra_flags=extra,
+                checked="--checked" in sys.argv))

@@ -14,6 +14,7 @@ __global__ void accept_kernel(int B, int D, const int32_t* __restrict__ parents,
                               const int32_t* __restrict__ target, int32_t* __restrict__ accept_len,
                               int32_t* __restrict__ path, int32_t* __restrict__ bonus,
                               int32_t* status) {
+  pdl_launch_dependents();   // the refresh may launch now; it waits for this kernel's results
   const int warps_per_block = blockDim.x / 32;
   const int b = blockIdx.x * warps_per_block + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;

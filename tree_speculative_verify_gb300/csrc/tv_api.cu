@@ -43,6 +43,7 @@ extern "C" const char* tv_status_string(int code) {
     case TV_ERR_WORKSPACE: return "TV_ERR_WORKSPACE";
     case TV_ERR_TIMEOUT: return "TV_ERR_TIMEOUT";
     case TV_ERR_SELECTION: return "TV_ERR_SELECTION";
+    case TV_ERR_BOUNDS: return "TV_ERR_BOUNDS";
     default: return "TV_ERR_UNKNOWN";
   }
 }
@@ -321,17 +322,15 @@ static tv::AttnParams<T> make_params(const tv_shape* s, const void* Q, const voi
   return p;
 }
 
-extern "C" int tv_tree_verify_attn(const tv_shape* s, const void* Q, const void* c4K,
-                                   const void* c4V, const int32_t* sel, const void* c128K,
-                                   const void* c128V, const void* rawK, const void* rawV,
-                                   const int32_t* L, const void* treeK, const void* treeV,
-                                   const uint64_t* anc, const int32_t* raw_lo,
-                                   const uint64_t* scr_vis4, const uint64_t* scr_vis128,
-                                   const void* scrK4, const void* scrV4, const void* scrK128,
-                                   const void* scrV128, float scale, void* O, float* lse,
-                                   void* workspace, size_t ws_bytes, int32_t* status,
-                                   tv_stream_t stream) {
-  const char* fn = "tv_tree_verify_attn";
+// The attention behind both entry points; fn names the caller's entry point in error messages.
+int tv_attn_entry(const char* fn, const tv_shape* s, const void* Q, const void* c4K,
+                  const void* c4V, const int32_t* sel, const void* c128K, const void* c128V,
+                  const void* rawK, const void* rawV, const int32_t* L, const void* treeK,
+                  const void* treeV, const uint64_t* anc, const int32_t* raw_lo,
+                  const uint64_t* scr_vis4, const uint64_t* scr_vis128, const void* scrK4,
+                  const void* scrV4, const void* scrK128, const void* scrV128, float scale,
+                  void* O, float* lse, void* workspace, size_t ws_bytes, int32_t* status,
+                  tv_stream_t stream) {
   if (int rc = check_shape(s, fn)) return rc;
   if (s->B == 0) return TV_OK;
   TV_REQUIRE(Q, fn);
@@ -398,6 +397,21 @@ extern "C" int tv_tree_verify_attn(const tv_shape* s, const void* Q, const void*
   p.chunk = sp.chunk;
   p.part = (float*)workspace;
   return tv_launch_attn_simt_f32(p, (cudaStream_t)stream);
+}
+
+extern "C" int tv_tree_verify_attn(const tv_shape* s, const void* Q, const void* c4K,
+                                   const void* c4V, const int32_t* sel, const void* c128K,
+                                   const void* c128V, const void* rawK, const void* rawV,
+                                   const int32_t* L, const void* treeK, const void* treeV,
+                                   const uint64_t* anc, const int32_t* raw_lo,
+                                   const uint64_t* scr_vis4, const uint64_t* scr_vis128,
+                                   const void* scrK4, const void* scrV4, const void* scrK128,
+                                   const void* scrV128, float scale, void* O, float* lse,
+                                   void* workspace, size_t ws_bytes, int32_t* status,
+                                   tv_stream_t stream) {
+  return tv_attn_entry("tv_tree_verify_attn", s, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L,
+                       treeK, treeV, anc, raw_lo, scr_vis4, scr_vis128, scrK4, scrV4, scrK128,
+                       scrV128, scale, O, lse, workspace, ws_bytes, status, stream);
 }
 
 extern "C" int tv_accept_walk(const tv_shape* s, const int32_t* parents, const int32_t* draft,

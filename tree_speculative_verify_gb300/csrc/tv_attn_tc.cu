@@ -103,6 +103,7 @@ struct Params {
   Paging pg;       // paged pools: C4 tiles are read through the page table; the C128 entries and
                    // the raw tail are first gathered into the workspace (contiguous per request)
   int tail_rows;   // rows per request of the gathered raw tail (paged pools only)
+  int64_t rows_c4, rows_c128, rows_raw;   // row extents of the C4, C128 and raw maps
   uint64_t timeout_ns;   // bound of every wait (kTimeoutNs unless a test shortens it)
   int withhold_tile;     // test aid: the producers never issue this tile's K copies (-1: none)
 };
@@ -373,6 +374,22 @@ __device__ __forceinline__ int64_t tile_row(const Params& p, int kind, int b, in
   return (int64_t)b * p.raw_cap + idx;
 }
 
+// Split-KV partial row of (request, row, chunk); the bounds-checked build confines it to the
+// workspace (row 0 on a violation).
+// (rows past D*H -- the last row tile's padding -- are never stored and are not checked)
+__device__ __forceinline__ int64_t part_row(const Params& p, int b, int grow, int chunk) {
+  const int64_t i = ((int64_t)b * p.DH + grow) * p.n_chunks + chunk;
+  if (grow >= p.DH) return i;
+  return tv_in_range(i, 0, (int64_t)p.B * p.DH * p.n_chunks, p.status, 4) ? i : 0;
+}
+
+// Bounds-checked build: a prefix tile's first row lies inside its map (rows past it, in the
+// padding of a ragged tile, are filled with zeros by the copy and masked).
+__device__ __forceinline__ bool tile_rows_ok(const Params& p, int kind, int64_t row) {
+  const int64_t n = kind == kC4 ? p.rows_c4 : kind == kC128 ? p.rows_c128 : p.rows_raw;
+  return tv_in_range(row, 0, n, p.status, 1);
+}
+
 // A descriptor's start-address field is (address >> 4) in its low 14 bits; every operand here
 // lies below 256 KB of shared memory, so adding (offset >> 4) never carries out of the field.
 __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_offset) {
@@ -466,7 +483,7 @@ __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
     if (it.tb >= it.te) continue;
     const int b = it.b;
     const Layout& y = it.y;
-    const int tree_row = b * p.D;
+    const int tree_row = tv_in_range(b * p.D, 0, p.tree_rows, p.status, 2) ? b * p.D : 0;
     // pair O: the previous item's epilogue stages O in the V ring; its slots are free again
     // once the role warps report v_free
     if (!role_s && q > 0 && !mbar_wait(&sm.h.v_free, (q - 1) & 1, &sm.h.abort, p.timeout_ns)) {
@@ -538,8 +555,12 @@ __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
               const CUtensorMap* m =
                   x.kind == kC4 ? &p.mC4K : x.kind == kC128 ? &p.mC128K : &p.mRawK;
               expect(kSlotBytes);
+              // (the follower loads the tile's second half, which may lie wholly in the padding
+              // past the map: checked is the leader's first row; a failed check still issues the
+              // copies, from row 0, so the barrier completes)
+              const int row = (sub == 1 || tile_rows_ok(p, x.kind, cur.x)) ? cur.x : 0;
               for (int ks = 0; ks < kKSlices; ++ks)
-                tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * g + ks), cur.x, bar);
+                tma_load_2d_pair(dst + ks * 8192, m, 64 * (kKSlices * g + ks), row, bar);
             }
           }
         } else if (lane == 0) {
@@ -559,10 +580,12 @@ __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
                 x.kind == kC4 ? &p.mC4V : x.kind == kC128 ? &p.mC128V : &p.mRawV;
             const int nvh = (x.nqk + 63) / 64;   // 64-row halves to load
             expect(nvh * 2 * 8192);
-            for (int h = 0; h < nvh; ++h)
+            for (int h = 0; h < nvh; ++h) {
+              const int hr = h == 0 ? cur.x : cur.y;
+              const int row = tile_rows_ok(p, x.kind, hr) ? hr : 0;
               for (int cb = 0; cb < 2; ++cb)
-                tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb,
-                                 h == 0 ? cur.x : cur.y, bar);
+                tma_load_2d_pair(dst + cb * kVBlock + h * 8192, m, col0 + 64 * cb, row, bar);
+            }
           }
         }
         finish(loads);
@@ -1031,7 +1054,7 @@ __device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
     const bool row_ok = grow < p.DH;
     if (n <= 0) {
       if (it.y.T > 0 && p.n_chunks > 1 && row_ok) {   // an empty KV chunk: l = 0
-        float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + it.chunk) * (d + 4);
+        float* prow = p.part + part_row(p, b, grow, it.chunk) * (d + 4);
         for (int c = 0; c < 256; c += 4)
           *reinterpret_cast<float4*>(prow + 256 * ch + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         if (ch == 0) {
@@ -1127,19 +1150,20 @@ __device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
           fail(sm, p.status);
           return;
         }
-        for (int j = 0; j < 8; ++j)
-          asm volatile(
-              "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::
-                  "l"(reinterpret_cast<uint64_t>(&p.mO)),
-              "r"(64 * j), "r"(128 * it.rt), "r"(b), "r"(smem_u32(stage + j * 16384))
-              : "memory");
+        if (tv_in_range(b, 0, p.B, p.status, 3) && tv_in_range(128 * it.rt, 0, p.DH, p.status, 3))
+          for (int j = 0; j < 8; ++j)
+            asm volatile(
+                "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+                    "l"(reinterpret_cast<uint64_t>(&p.mO)),
+                "r"(64 * j), "r"(128 * it.rt), "r"(b), "r"(smem_u32(stage + j * 16384))
+                : "memory");
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         mbar_arrive(&sm.h.v_free);
       }
       continue;
     } else {
-      float* prow = p.part + (((int64_t)b * p.DH + grow) * p.n_chunks + it.chunk) * (d + 4);
+      float* prow = p.part + part_row(p, b, grow, it.chunk) * (d + 4);
       for (int c = 0; c < 256 / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_base + 256 * ch + 32 * c, r);
@@ -1491,6 +1515,9 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
     c128V = rawV;
   }
   const uint64_t trows = B * (uint64_t)s->D;
+  p.rows_c4 = (int64_t)c4rows;
+  p.rows_c128 = (int64_t)c128rows;
+  p.rows_raw = (int64_t)rawrows;
   bool ok = make_map(&p.mQ, a.Q, 3, DH, B, 128) && make_map(&p.mO, a.O, 3, DH, B, 128);
   ok = ok && make_map(&p.mC4K, c4K, 2, c4rows, 1, 64) && make_map(&p.mC4V, c4V, 2, c4rows, 1, 64);
   ok = ok && make_map(&p.mC128K, c128K, 2, c128rows, 1, 64) &&

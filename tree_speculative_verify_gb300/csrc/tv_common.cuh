@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include "treeverify.h"
 
@@ -41,6 +42,32 @@ __device__ __forceinline__ float warp_max(float x) {
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
 }
+
+// Range checks of the bounds-checked build (compiled with -DTV_CHECK_BOUNDS, see build.py): a global
+// index computed on the device must satisfy lo <= i < hi before the access it addresses.  A
+// violation records TV_ERR_BOUNDS in the status word, prints the site number and the index (from
+// the thread that recorded it), and the caller skips the access.  In the normal build the check
+// is the constant true and costs nothing.  Sites:
+//   1 attention producer, first row of a prefix tile inside its map
+//   2 attention producer, the request's tree / scratch rows
+//   3 attention epilogue, O rows                  4 attention epilogue, split-KV partial rows
+//   5 a persistent row (raw, C4, C128) inside its request's capacity (layer_row, contiguous
+//     layout: prefill, scratch pad, refresh, selection gather); the paged layout checks its page
+//     ids against the pool and reports TV_ERR_ARG in every build
+#ifdef TV_CHECK_BOUNDS
+__device__ __forceinline__ bool tv_in_range(int64_t i, int64_t lo, int64_t hi, int32_t* status,
+                                            int site) {
+  if (i >= lo && i < hi) return true;
+  if (status != nullptr && atomicCAS(status, 0, TV_ERR_BOUNDS) == 0)
+    printf("treeverify bounds check: site %d index %lld not in [%lld, %lld) (block %d, thread %d)\n",
+           site, (long long)i, (long long)lo, (long long)hi, (int)blockIdx.x, (int)threadIdx.x);
+  return false;
+}
+#else
+__device__ __forceinline__ constexpr bool tv_in_range(int64_t, int64_t, int64_t, int32_t*, int) {
+  return true;
+}
+#endif
 
 // Programmatic dependent launch.  A kernel launched with launch_pdl may start while the kernel
 // before it in the stream still runs, once every CTA of that kernel has called
@@ -104,7 +131,8 @@ inline Paging paging_of(const tv_shape* s) {
 // clamped to its last row, so the page-table read stays inside the request's row of the table.
 __device__ __forceinline__ int64_t layer_row(const Paging& pg, int b, int64_t idx, int64_t cap,
                                              int tokens_per_row, int32_t* status) {
-  if (pg.page_tokens == 0) return (int64_t)b * cap + idx;
+  if (pg.page_tokens == 0)
+    return (int64_t)b * cap + (tv_in_range(idx, 0, cap, status, 5) ? idx : 0);
   if (idx >= cap) idx = cap - 1;
   if (idx < 0) idx = 0;
   const int64_t rpp = pg.page_tokens / tokens_per_row;
@@ -120,4 +148,13 @@ __device__ __forceinline__ int64_t layer_row(const Paging& pg, int b, int64_t id
 
 // Host-side helpers shared by the entry points (defined in tv_api.cu).
 int tv_set_error(int code, const char* fmt, ...);
+// tv_tree_verify_attn's body; fn names the public entry point in error messages.
+int tv_attn_entry(const char* fn, const tv_shape* s, const void* Q, const void* c4K,
+                  const void* c4V, const int32_t* sel, const void* c128K, const void* c128V,
+                  const void* rawK, const void* rawV, const int32_t* L, const void* treeK,
+                  const void* treeV, const uint64_t* anc, const int32_t* raw_lo,
+                  const uint64_t* scr_vis4, const uint64_t* scr_vis128, const void* scrK4,
+                  const void* scrV4, const void* scrK128, const void* scrV128, float scale,
+                  void* O, float* lse, void* workspace, size_t ws_bytes, int32_t* status,
+                  tv_stream_t stream);
 int tv_check_launch(const char* what);

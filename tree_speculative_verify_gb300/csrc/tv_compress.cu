@@ -631,6 +631,8 @@ __global__ void refresh_kernel(Paging pg, int D, int d, int es, int comp_mask, i
                                const char* scrK128, const char* scrV128, char* rawK, char* rawV,
                                char* c4K, char* c4V, char* c128K, char* c128V, int32_t* L,
                                int32_t* committed, int32_t* status) {
+  // launched as a programmatic dependent of the acceptance walk, whose results it reads
+  pdl_wait();
   constexpr int kSlots = 3 * kMaxD;
   __shared__ const char* s_srcK[kSlots];
   __shared__ const char* s_srcV[kSlots];
@@ -840,11 +842,16 @@ int tv_launch_refresh(const tv_shape* s, const int32_t* parents, const int32_t* 
                       void* c4K, void* c4V, void* c128K, void* c128V, int32_t* L,
                       int32_t* committed, int32_t* status, cudaStream_t stream) {
   const int es = s->dtype == TV_BF16 ? 2 : 4;
-  tv::refresh_kernel<<<s->B, 256, 0, stream>>>(
-      tv::paging_of(s), s->D, s->d, es, s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap,
-      s->stage_chain, parents, accept_len, path,
-      (const char*)treeK, (const char*)treeV, (const char*)scrK4, (const char*)scrV4,
-      (const char*)scrK128, (const char*)scrV128, (char*)rawK, (char*)rawV, (char*)c4K,
-      (char*)c4V, (char*)c128K, (char*)c128V, L, committed, status);
+  const cudaError_t e = tv::launch_pdl(
+      tv::refresh_kernel, dim3(s->B), dim3(256), 0, stream, tv::paging_of(s), s->D, s->d, es,
+      s->comp_mask, s->raw_cap, s->c4_cap, s->c128_cap, (int)s->stage_chain, parents,
+      accept_len, path, (const char*)treeK, (const char*)treeV, (const char*)scrK4,
+      (const char*)scrV4, (const char*)scrK128, (const char*)scrV128, (char*)rawK, (char*)rawV,
+      (char*)c4K, (char*)c4V, (char*)c128K, (char*)c128V, L, committed, status);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return tv_set_error(TV_ERR_CUDA, "tv_refresh_commit: launch failed: %s",
+                        cudaGetErrorString(e));
+  }
   return tv_check_launch("tv_refresh_commit");
 }

@@ -10,51 +10,44 @@
 // the library image itself, so it never allocates.
 //
 // The scratch array is a file-scope __device__ array of kNoAllocScratchBytes (32 MiB): every GPU
-// that loads the library holds it until the process exits.  Calls whose shape needs more scratch
+// that loads the library's device code holds it until the process exits.  With CUDA's lazy module
+// loading (the default) that happens at the first call on each device that resolves the array --
+// tv_noalloc_prepare or the first tv_tree_verify_attn_noalloc -- so a caller that hands all free
+// memory to its own pool makes one of those calls first.  Calls whose shape needs more scratch
 // than that (see tv_workspace_size) are rejected with TV_ERR_WORKSPACE.  All calls share the
 // array, so calls that overlap on the GPU (different streams, or different threads without
 // ordering) race on it; the kernels write every partial result they later read, so nothing in it
-// needs to start at zero and the contents left by the previous call are never used.
-#include <mutex>
-
+// needs to start at zero and the contents left by the previous call are never used.  The array's
+// address is looked up on every call, in the caller's current context, so it stays right across a
+// device reset or a change of context.
 #include "tv_common.cuh"
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  Resolved once per device, on the
-// first call made with that device current (host code cannot use the array's name as a device
-// address: it is a host-side stand-in for the symbol).
-int scratch_for_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+// Device address of the scratch array in the current context (host code cannot use the array's
+// name as a device address: it is a host-side stand-in for the symbol).
+int scratch_address(const char* fn, void** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
     cudaGetLastError();
-    return tv_set_error(TV_ERR_CUDA, "tv_tree_verify_attn_noalloc: no current CUDA device");
+    return tv_set_error(TV_ERR_CUDA, "%s: the built-in scratch is not available: %s", fn,
+                        cudaGetErrorString(e));
   }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return tv_set_error(TV_ERR_CUDA,
-                          "tv_tree_verify_attn_noalloc: cudaGetSymbolAddress failed: %s",
-                          cudaGetErrorString(e));
-    }
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return TV_OK;
 }
 
 }  // namespace
+
+extern "C" int tv_noalloc_prepare(void) {
+  void* p = nullptr;
+  return scratch_address("tv_noalloc_prepare", &p);
+}
 
 extern "C" int tv_tree_verify_attn_noalloc(
     const tv_shape* s, const void* Q, const void* c4K, const void* c4V, const int32_t* sel,
@@ -63,17 +56,17 @@ extern "C" int tv_tree_verify_attn_noalloc(
     const uint64_t* scr_vis4, const uint64_t* scr_vis128, const void* scrK4, const void* scrV4,
     const void* scrK128, const void* scrV128, float scale, void* O, float* lse, int32_t* status,
     tv_stream_t stream) {
-  if (s == nullptr)
-    return tv_set_error(TV_ERR_ARG, "tv_tree_verify_attn_noalloc: shape is null");
+  const char* fn = "tv_tree_verify_attn_noalloc";
+  if (s == nullptr) return tv_set_error(TV_ERR_ARG, "%s: shape is null", fn);
   const size_t need = tv_workspace_size(s);
   if (need > kNoAllocScratchBytes)
     return tv_set_error(TV_ERR_WORKSPACE,
-                        "tv_tree_verify_attn_noalloc: this shape needs %zu bytes of scratch; the "
-                        "built-in scratch holds %zu (use tv_tree_verify_attn with a workspace)",
-                        need, kNoAllocScratchBytes);
+                        "%s: this shape needs %zu bytes of scratch; the built-in scratch holds "
+                        "%zu (use tv_tree_verify_attn with a workspace)",
+                        fn, need, kNoAllocScratchBytes);
   void* scratch = nullptr;
-  if (int rc = scratch_for_current_device(&scratch)) return rc;
-  return tv_tree_verify_attn(s, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L, treeK, treeV, anc,
-                             raw_lo, scr_vis4, scr_vis128, scrK4, scrV4, scrK128, scrV128, scale,
-                             O, lse, scratch, kNoAllocScratchBytes, status, stream);
+  if (int rc = scratch_address(fn, &scratch)) return rc;
+  return tv_attn_entry(fn, s, Q, c4K, c4V, sel, c128K, c128V, rawK, rawV, L, treeK, treeV, anc,
+                       raw_lo, scr_vis4, scr_vis128, scrK4, scrV4, scrK128, scrV128, scale, O,
+                       lse, scratch, kNoAllocScratchBytes, status, stream);
 }
