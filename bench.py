@@ -803,8 +803,10 @@ def launches_per_step(shape, kernel):
         return 6 + (2 if shape.n_sel > 0 else 0)
     gather = shape.B * shape.n_sel * 512 * 2 * 2
     split = _lib.tv_workspace_size(shape) > ((shape.B * 4 + 255) // 256) * 256 + gather
-    # + the indexer's score and select kernels and the selection gather on the sparse path
-    return 4 + 2 + (1 if split else 0) + (3 if shape.n_sel > 0 else 0)
+    # + the indexer's score and select kernels and the selection gather on the sparse path, and
+    # the gather of the C128 entries and raw tails from page pools
+    return (4 + 2 + (1 if split else 0) + (3 if shape.n_sel > 0 else 0)
+            + (1 if shape.page_tokens > 0 else 0))
 
 
 def main():

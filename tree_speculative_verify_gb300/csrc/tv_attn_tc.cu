@@ -7,14 +7,18 @@
 // heads sharing one K/V head, all D*H query rows of a request read the same compressed prefix, so
 // the prefix part is a dense (D*H) x entries x 512 contraction -- tensor-core work.
 //
-// Work item: a cluster of four CTAs for request b, two consecutive 128-row tiles of the request's
-// D*H query rows (node-major) and one chunk of the request's KV tiles.  The cluster is two CTA
-// pairs that split the work of every KV tile by stage rather than by data:
+// Work item: request b, two consecutive 128-row tiles of the request's D*H query rows
+// (node-major) and one chunk of the request's KV tiles.  A persistent grid holds one cluster of
+// four CTAs per resident cluster slot; cluster c walks the longest-first item list in a snake
+// order (item c, then 2G-1-c, 2G+c, ...), and tile counters run across its items, so barriers,
+// TMEM and the rings are set up once.  The cluster is two CTA pairs that split the work of every
+// KV tile by stage rather than by data:
 //   pair S (ranks 0-1)   S_t = Q K_t^T with cta_group::2 MMAs (M = 256: each CTA's tensor core on
 //                        its own 128 rows; N = tile entries; K = 512, A = Q from TMEM, B = K from
 //                        shared memory, split between the two CTAs), then the online softmax; each
-//                        CTA sends its rows' bf16 P_t to the CTA of the other pair that holds the
-//                        same rows, into that CTA's shared memory (st.async)
+//                        CTA stages its rows' bf16 P_t (with the rows' rescale factors) and one bulk
+//                        shared-memory copy takes it to the CTA of the other pair that holds the
+//                        same rows
 //   pair O (ranks 2-3)   O += P_t V_t with cta_group::2 MMAs (A = P from shared memory, B = V,
 //                        N = 2 x 256 value columns), O for all 512 columns in TMEM
 // A 128-row fp32 O of all 512 columns fills the 512 TMEM columns of a CTA, so S and O cannot share
@@ -27,24 +31,29 @@
 // KV tiles (<= 128 entries each), in order: persistent C4 entries, persistent C128 entries, the raw
 // tail (positions t0 .. L-1), and one "extra" tile of 32 entries: the tree tokens (0..7), the C4
 // scratch rows (8..15), the C128 scratch rows (16..23) and 8 zero rows.  Shared tiles are visible
-// to every row; raw and extra tiles are filtered per tree node with the plan (raw_lo, ancestor
-// mask, scratch visibility) inside the softmax warps.
+// to every row; raw and extra tiles are filtered per tree node inside the softmax warps with a
+// 64-bit column mask per row built from the plan (raw_lo, ancestor mask, scratch visibility).
 //
 // Warp roles (352 threads per CTA):
-//   warp 0      TMA producer: pair S, this CTA's half of every tile's K entries x 512 dims (two
-//               32 KB slots of a 6-slot ring); pair O, the tile's entries x this CTA's 256 value
-//               columns (two 32 KB slots of a 4-slot ring).  All copies of a pair complete on its
-//               leader's barriers (cta_group::2 TMA).
+//   warp 0      TMA producer: pair S, the item's Q rows (through four ring slots, then copied into
+//               TMEM) and this CTA's half of every tile's K entries x 512 dims (two 32 KB slots of
+//               a 5-slot ring); pair O, the tile's entries x this CTA's 256 value columns (two
+//               32 KB slots of a 4-slot ring).  All copies of a pair complete on its leader's
+//               barriers (cta_group::2 TMA).
 //   warp 1      both CTAs: allocate / free 512 TMEM columns (cta_group::2); the leader's lane 0
 //               issues the pair's MMAs and releases ring slots and buffers with multicast commits
 //   warps 2..9  pair S: Q rows into TMEM, then per tile the softmax, two threads per query row
 //               (one per half of the tile's columns) sharing one running maximum; pair O: per
-//               tile the (rare) O rescale, and at the end O / l out through TMA stores
+//               tile the (rare) O rescale, and at the end of an item O / l out through TMA stores
+//               from a staging copy in the idle V ring
 //   warp 10     lane 0: forwards this CTA's per-tile readiness to its pair leader (leader: local
-//               arrive with expect_tx; follower: a 4-byte st.async)
+//               arrive with expect_tx; follower: a 4-byte st.async), and moves P to pair O
 // TMEM columns: pair S: S buffers at [0,128) and [128,256), Q at [256,512); pair O: O at [0,512).
 // Every wait is bounded; on timeout the CTA records TV_ERR_TIMEOUT, sets the abort flag of all
 // four CTAs, stops issuing work, drains its own copies and MMAs (bounded) and frees its TMEM.
+// The kernel is a programmatic dependent of the scheduling kernel: its set-up (barriers, TMEM,
+// tensor-map prefetch) overlaps that kernel, and it reads the round's inputs only after it.
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
