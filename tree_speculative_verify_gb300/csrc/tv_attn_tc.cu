@@ -961,18 +961,32 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
           vmask = (hi == 64 ? ~0ull : ((1ull << hi) - 1ull)) & ~((1ull << lo) - 1ull);
         }
         const uint32_t vlo = (uint32_t)vmask, vhi = (uint32_t)(vmask >> 32);
-        // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows)
-        float mx[8];
+        // row maximum of the visible raw logits (scale > 0, so the scaled maximum follows); the
+        // softmax warps' instructions compete with the MMA issuer for the SM's issue slots, so a
+        // fully visible half-row (most tiles) takes a three-input maximum tree
+        if (vmask == ~0ull) {
+          float t[22];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
+          for (int j = 0; j < 21; ++j) t[j] = max3f(s[3 * j], s[3 * j + 1], s[3 * j + 2]);
+          t[21] = s[63];
+          float u[8];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const bool vis = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
-          s[j] = vis ? s[j] : -INFINITY;
-          mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+          for (int j = 0; j < 7; ++j) u[j] = max3f(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
+          u[7] = t[21];
+          raw_max = max3f(max3f(u[0], u[1], u[2]), max3f(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+        } else {
+          float mx[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mx[j] = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const bool vis = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
+            s[j] = vis ? s[j] : -INFINITY;
+            mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+          }
+          raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         }
-        raw_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       }
       sm.h.xmax[sb][ch][row] = raw_max;
       if (lane == 0) sm.h.xok[sb][ch][quad] = ok ? 1 : 0;
@@ -989,19 +1003,24 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
       // exactly 1 unless the maximum grows past a finite reference: pair O rescales O by it
       const float alpha = (grow_max && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
       const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
-      float sum[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sum[j] = 0.f;
+      // exponent arguments and partial sums two at a time (packed fp32 pairs)
+      const uint64_t scale2 = pack_f32x2(sl2, sl2), shift2 = pack_f32x2(neg_m, neg_m);
+      uint64_t sum2[2] = {pack_f32x2(0.f, 0.f), pack_f32x2(0.f, 0.f)};
       uint32_t pk[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float p0 = ex2_approx(fmaf(s[2 * j], sl2, neg_m));
-        const float p1 = ex2_approx(fmaf(s[2 * j + 1], sl2, neg_m));
-        sum[j & 3] += p0 + p1;
+        float a0, a1;
+        unpack_f32x2(fma_f32x2(pack_f32x2(s[2 * j], s[2 * j + 1]), scale2, shift2), a0, a1);
+        const float p0 = ex2_approx(a0);
+        const float p1 = ex2_approx(a1);
+        sum2[j & 1] = add_f32x2(sum2[j & 1], pack_f32x2(p0, p1));
         const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
         pk[j] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      const float tsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      float s0, s1, s2, s3;
+      unpack_f32x2(sum2[0], s0, s1);
+      unpack_f32x2(sum2[1], s2, s3);
+      const float tsum = (s0 + s1) + (s2 + s3);
       l_run = l_run * alpha + tsum;
       m_ref = m_new;
       // the copy of P_{g-1} has read the staging buffer
