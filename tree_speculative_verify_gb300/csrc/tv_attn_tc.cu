@@ -1417,17 +1417,21 @@ int tc_chunks(const tv_shape* s) {
   if (s->comp_mask & TV_COMP_C4) max_tiles += ((s->n_sel > 0 ? s->n_sel : s->c4_cap) + 127) / 128;
   if (s->comp_mask & TV_COMP_C128) max_tiles += (s->c128_cap + 127) / 128;
   const int64_t clusters1 = (int64_t)s->B * n_pairs_of(s);
-  int best = 1;
+  // makespan in tile periods: waves of items x (tiles per chunk + an item's fill and drain, about
+  // kItemTiles tile periods); the fewest chunks within 10 % of the best (every chunk adds a
+  // partial row per query row to write and merge)
+  constexpr int64_t kItemTiles = 12;
+  int64_t cost[65];
   int64_t best_cost = -1;
-  for (int n = 1; n <= 64 && n <= max_tiles; ++n) {
+  const int n_max = (int)(max_tiles < 64 ? max_tiles : 64);
+  for (int n = 1; n <= n_max; ++n) {
     const int64_t waves = (clusters1 * n + slots - 1) / slots;
-    const int64_t cost = waves * ((max_tiles + n - 1) / n + 4);
-    if (best_cost < 0 || 10 * cost < 9 * best_cost) {
-      best_cost = cost;
-      best = n;
-    }
+    cost[n] = waves * ((max_tiles + n - 1) / n + kItemTiles);
+    if (best_cost < 0 || cost[n] < best_cost) best_cost = cost[n];
   }
-  return best;
+  for (int n = 1; n <= n_max; ++n)
+    if (10 * cost[n] <= 11 * best_cost) return n;
+  return 1;
 }
 
 // Test aid (tv_debug_attn_timeout): the bound of every wait and one KV tile whose K copies the
