@@ -11,13 +11,17 @@
 // sum in index order i = 0 .. d_idx-1 with one round-to-nearest-even per addition and no fused
 // multiply-add (__fmul_rn / __fadd_rn).
 //
-// Two kernels:
-//   score_kernel   one thread per (request, entry): the fp32 score into the workspace.
-//   select_kernel  one 1024-thread CTA per request: an 8-bit-digit radix select (four passes over
-//                  the request's scores, shared-memory histograms) finds the n_sel-th largest key;
-//                  then every warp counts the entries above it and the ties in its contiguous
-//                  index range (32 consecutive keys per step), the warps' counts place its kept
-//                  entries, and it writes them in ascending order (ties: the lowest indices).
+// One kernel, a cluster of eight CTAs per request; CTA r owns the request's r-th contiguous eighth
+// of the C4 entries:
+//   1. scores of its entries -> order-preserving keys in shared memory, the indexer keys
+//      streamed through shared memory in contiguous tiles, several in flight, one thread per row;
+//   2. an 8-bit-digit radix select of the n_sel-th largest key over the whole request: per pass
+//      every CTA counts its keys into a shared-memory histogram, and after one cluster barrier each
+//      CTA sums the eight histograms through distributed shared memory and picks the same digit;
+//   3. the kept entries in ascending order: every warp counts the entries above the threshold and
+//      the ties in its contiguous index range, CTAs in rank order and warps in index order place
+//      them (ties: the lowest indices), and each warp writes its own.
+#include <cooperative_groups.h>
 #include <mutex>
 
 #include "tv_common.cuh"
@@ -25,10 +29,24 @@
 namespace tv {
 namespace {
 
-constexpr int kSelThreads = 1024;
-// Keys staged in shared memory when a request has at most this many C4 entries (160 KB): the four
-// radix passes and the final pass then read shared memory instead of re-reading the scores.
-constexpr int kSmemKeys = 40960;
+constexpr int kTopkRanks = 8;        // CTAs per request (one cluster)
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+// Keys a CTA stages in shared memory (24 KB, beside three 64 KB key tiles and the static arrays):
+// its share of a request of up to 8 x 6144 C4 entries.  A larger share keeps its scores in the
+// workspace and re-reads them in each pass.
+constexpr int kStageKeys = 6144;
+constexpr int kMaxIdxVec = 64;       // 16-byte vectors of the indexer query (d_idx <= 512)
+constexpr int kKeyTileBytes = 65536; // indexer keys staged per tile
+constexpr int kKeyTiles = 3;         // tiles in flight
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_two() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_none() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Order-preserving map of an fp32 score to an unsigned key (larger score -> larger key); -0 and
 // +0 map to the same key.
@@ -41,82 +59,148 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__global__ void score_kernel(int B, int64_t c4_cap, int d_idx, const uint16_t* __restrict__ q_idx,
-                             const uint16_t* __restrict__ k_idx, const int32_t* __restrict__ L,
-                             float* __restrict__ score) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= (int64_t)B * c4_cap) return;
-  const int b = (int)(t / c4_cap);
-  const int64_t j = t - (int64_t)b * c4_cap;
-  const int Lb = L[b];
-  if (Lb < 0 || j >= Lb / 4) return;
-  const uint4* q = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx);
-  const uint4* k = reinterpret_cast<const uint4*>(k_idx + t * d_idx);
-  float s = 0.f;
-  for (int c = 0; c < d_idx / 8; ++c) {
-    const uint4 qa = q[c], ka = k[c];
-    const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {   // element 2h (low half) before 2h+1 (high half)
-      s = __fadd_rn(s, __fmul_rn(bf16_lo(qw[h]), bf16_lo(kw[h])));
-      s = __fadd_rn(s, __fmul_rn(bf16_hi(qw[h]), bf16_hi(kw[h])));
-    }
-  }
-  score[t] = s;
-}
-
-// The radix select and the ordered write for one request of n4 keys.  kStaged: the keys are in
-// shared memory (read four at a time in the histogram passes); otherwise each pass re-reads the
-// scores.  The shared-memory arrays come from the kernel.
-template <bool kStaged>
-__device__ __forceinline__ void select_request(int n4, int n_sel, const uint32_t* keys_smem,
-                                               const float* __restrict__ sc,
-                                               int32_t* __restrict__ out, unsigned* hist,
-                                               int* warp_gt, int* warp_eq, uint32_t* s_prefix,
-                                               uint32_t* s_mask, int* s_krem) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// grid (8, B), clusters of 8 along x.  score_ws: [B][c4_cap] fp32, used only when a CTA's share
+// exceeds kStageKeys.
+__global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThreads)
+    topk_kernel(int64_t c4_cap, int d_idx, int n_sel, const uint16_t* __restrict__ q_idx,
+                const uint16_t* __restrict__ k_idx, const int32_t* __restrict__ L,
+                float* __restrict__ score_ws, int32_t* __restrict__ sel, int32_t* status) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  extern __shared__ __align__(16) uint32_t smem_dyn[];
+  // kKeyTiles tiles of indexer keys in flight, then this CTA's keys (when staged)
+  uint4* ktile = reinterpret_cast<uint4*>(smem_dyn);
+  uint32_t* keys = smem_dyn + kKeyTiles * kKeyTileBytes / 4;
+  __shared__ uint4 q[kMaxIdxVec];
+  __shared__ unsigned hist[2][256];   // by pass parity (a rank that runs ahead never clears a
+                                      // histogram a slower rank still reads)
+  __shared__ unsigned ghist[256];     // the pass's histogram of the whole request
+  __shared__ int warp_gt[kTopkWarps], warp_eq[kTopkWarps];
+  __shared__ int cta_gt, cta_eq;
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_krem;
+  const int b = blockIdx.y;
+  const int rank = (int)cl.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  auto key_at = [&](int j) -> uint32_t { return kStaged ? keys_smem[j] : score_key(sc[j]); };
-  if (threadIdx.x == 0) {
-    *s_prefix = 0u;
-    *s_mask = 0u;
-    *s_krem = n_sel;
+  const int Lb = L[b];
+  const int64_t n4l = Lb >= 0 ? Lb / 4 : -1;
+  int32_t* out = sel + (int64_t)b * n_sel;
+  if (n4l < n_sel || n4l > c4_cap) {   // uniform over the cluster
+    if (rank == 0) {
+      if (tid == 0) record_error(status, n4l > c4_cap ? TV_ERR_CAPACITY : TV_ERR_SELECTION);
+      for (int i = tid; i < n_sel; i += blockDim.x) out[i] = -1;
+    }
+    return;
+  }
+  const int n4 = (int)n4l;   // < 2^31: the shape check bounds B * c4_cap
+  const int per = (n4 + kTopkRanks - 1) / kTopkRanks;
+  const int lo = min(n4, rank * per), hi = min(n4, lo + per), n = hi - lo;
+  const bool staged = per <= kStageKeys;   // uniform over the cluster
+  float* sc = score_ws + (int64_t)b * c4_cap;
+  const int nvec = d_idx / 8;
+  // 1. scores of this CTA's entries -> keys
+  if (tid < nvec) q[tid] = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx)[tid];
+  if (tid == 0) {
+    s_prefix = 0u;
+    s_mask = 0u;
+    s_krem = n_sel;
   }
   __syncthreads();
-  // radix select of the n_sel-th largest key, most significant digit first (shared-memory atomics
-  // measured faster here than merging equal bins within a warp first)
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0u;
+  // the CTA's indexer keys stream through shared memory in tiles of RT rows, read as contiguous
+  // 16-byte chunks (kKeyTiles tiles in flight); chunk c of row r sits at r * nvec + (c ^ (r & 7)) when
+  // nvec is a multiple of 8, so the threads' row-wise reads do not collide on banks; thread r then
+  // forms row r's score with the (strictly ordered) additions
+  const int RT = kKeyTileBytes / (16 * nvec);
+  const int swz = (nvec & 7) == 0 ? 7 : 0;
+  const uint4* kbase = reinterpret_cast<const uint4*>(k_idx + ((int64_t)b * c4_cap + lo) * d_idx);
+  const int n_tiles = (n + RT - 1) / RT;
+  auto issue = [&](int tile) {
+    if (tile < n_tiles) {
+      uint4* dst = ktile + (tile % kKeyTiles) * (kKeyTileBytes / 16);
+      const int rows = min(RT, n - tile * RT);
+      const uint4* src = kbase + (int64_t)tile * RT * nvec;
+      for (int i = tid; i < rows * nvec; i += blockDim.x) {
+        const int r = i / nvec, c = i - r * nvec;
+        cp_async16(dst + r * nvec + (c ^ (r & swz)), src + i);
+      }
+    }
+    cp_async_commit();
+  };
+  issue(0);
+  issue(1);
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    issue(tile + 2);
+    cp_async_wait_two();   // this tile's copies have landed; the next two may be in flight
     __syncthreads();
-    const uint32_t prefix = *s_prefix, mask = *s_mask;
+    const uint4* kt = ktile + (tile % kKeyTiles) * (kKeyTileBytes / 16);
+    const int rows = min(RT, n - tile * RT);
+    for (int r = tid; r < rows; r += blockDim.x) {
+      float sacc = 0.f;
+      for (int c = 0; c < nvec; ++c) {
+        const uint4 qa = q[c], ka = kt[r * nvec + (c ^ (r & swz))];
+        const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {   // element 2h (low half) before 2h+1 (high half)
+          sacc = __fadd_rn(sacc, __fmul_rn(bf16_lo(qw[h]), bf16_lo(kw[h])));
+          sacc = __fadd_rn(sacc, __fmul_rn(bf16_hi(qw[h]), bf16_hi(kw[h])));
+        }
+      }
+      const int j = lo + tile * RT + r;
+      if (staged)
+        keys[j - lo] = score_key(sacc);
+      else
+        sc[j] = sacc;
+    }
+    __syncthreads();   // the tile's buffer may be refilled
+  }
+  cp_async_wait_none();
+  if (staged && tid < ((-n) & 3)) keys[n + tid] = 0u;   // whole 16-byte vectors
+  __syncthreads();
+  auto key_at = [&](int j) -> uint32_t { return staged ? keys[j - lo] : score_key(sc[j]); };
+  // 2. radix select of the n_sel-th largest key of the request, most significant digit first
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass, par = pass & 1;
+    for (int i = tid; i < 256; i += blockDim.x) hist[par][i] = 0u;
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
     auto count = [&](uint32_t key) {
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      if ((key & mask) == prefix) atomicAdd(&hist[par][(key >> shift) & 255u], 1u);
     };
-    if (kStaged) {
-      // four keys per 16-byte load; keys past n4 in the last vector are not counted
-      const uint4* k4 = reinterpret_cast<const uint4*>(keys_smem);
-      const int n16 = (n4 + 3) >> 2;
-      for (int q = threadIdx.x; q < n16; q += blockDim.x) {
-        const uint4 v = k4[q];
-        const int j = 4 * q;
-        count(v.x);
-        if (j + 1 < n4) count(v.y);
-        if (j + 2 < n4) count(v.z);
-        if (j + 3 < n4) count(v.w);
+    if (staged) {
+      const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+      for (int v = tid; v < (n + 3) >> 2; v += blockDim.x) {
+        const uint4 x = k4[v];
+        const int j = 4 * v;
+        count(x.x);
+        if (j + 1 < n) count(x.y);
+        if (j + 2 < n) count(x.z);
+        if (j + 3 < n) count(x.w);
       }
     } else {
-      for (int j = threadIdx.x; j < n4; j += blockDim.x) count(score_key(sc[j]));
+      for (int j = lo + tid; j < hi; j += blockDim.x) count(score_key(sc[j]));
+    }
+    __syncthreads();
+    cl.sync();   // every rank's histogram of this pass is complete
+    if (tid < 256) {   // bin tid summed over the ranks (their loads in flight together)
+      unsigned v[kTopkRanks];
+#pragma unroll
+      for (int r = 0; r < kTopkRanks; ++r) v[r] = *cl.map_shared_rank(&hist[par][tid], r);
+      unsigned t = 0u;
+#pragma unroll
+      for (int r = 0; r < kTopkRanks; ++r) t += v[r];
+      ghist[tid] = t;
     }
     __syncthreads();
     if (warp == 0) {
       // lane l holds bins 255-8l .. 248-8l (descending); an inclusive scan over lanes gives the
       // count of keys in the digits above each lane's group
-      const int krem = *s_krem;
+      const int krem = s_krem;
       int c[8], sum = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        c[q] = (int)hist[255 - 8 * lane - q];
-        sum += c[q];
+      for (int qd = 0; qd < 8; ++qd) {
+        c[qd] = (int)ghist[255 - 8 * lane - qd];
+        sum += c[qd];
       }
       int incl = sum;
 #pragma unroll
@@ -128,50 +212,72 @@ __device__ __forceinline__ void select_request(int n4, int n_sel, const uint32_t
       const unsigned hit = __ballot_sync(0xffffffffu, excl < krem && incl >= krem);
       if (lane == __ffs(hit) - 1) {
         int above = excl, digit = 0;
-        for (int q = 0; q < 8; ++q) {
-          if (above + c[q] >= krem) {
-            digit = 255 - 8 * lane - q;
+        for (int qd = 0; qd < 8; ++qd) {
+          if (above + c[qd] >= krem) {
+            digit = 255 - 8 * lane - qd;
             break;
           }
-          above += c[q];
+          above += c[qd];
         }
-        *s_krem = krem - above;
-        *s_prefix = prefix | ((uint32_t)digit << shift);
-        *s_mask = mask | (255u << shift);
+        s_krem = krem - above;
+        s_prefix = prefix | ((uint32_t)digit << shift);
+        s_mask = mask | (255u << shift);
       }
     }
     __syncthreads();
   }
-  const uint32_t T = *s_prefix;   // key of the n_sel-th best entry
-  const int need_eq = *s_krem;    // entries with key == T to keep: the lowest-indexed ones
-  // warp w owns the contiguous index range [w * R, (w + 1) * R), read 32 consecutive keys at a
-  // time: count, one scan over the warps, then write the kept entries in ascending order
-  const int n_warps = blockDim.x >> 5;
-  const int R = (n4 + n_warps - 1) / n_warps;
-  const int lo = warp * R, hi = lo + R < n4 ? lo + R : n4;
+  const uint32_t T = s_prefix;   // key of the n_sel-th best entry
+  const int need_eq = s_krem;    // entries with key == T to keep: the lowest-indexed ones
+  // 3. warp w owns the contiguous range [lo + w R, lo + (w + 1) R) of this CTA's entries, read 32
+  //    consecutive keys at a time: counts, placed over the CTAs (rank order) and the warps
+  const int R = (n + kTopkWarps - 1) / kTopkWarps;
+  const int wlo = lo + min(n, warp * R), whi = lo + min(n, warp * R + R);
   int gt = 0, eq = 0;
-  for (int j0 = lo; j0 < hi; j0 += 32) {
+  for (int j0 = wlo; j0 < whi; j0 += 32) {
     const int j = j0 + lane;
-    const uint32_t key = j < hi ? key_at(j) : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, j < hi && key > T));
-    eq += __popc(__ballot_sync(0xffffffffu, j < hi && key == T));
+    const uint32_t key = j < whi ? key_at(j) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, j < whi && key > T));
+    eq += __popc(__ballot_sync(0xffffffffu, j < whi && key == T));
   }
   if (lane == 0) {
     warp_gt[warp] = gt;
     warp_eq[warp] = eq;
   }
   __syncthreads();
+  if (tid == 0) {
+    int a = 0, e = 0;
+    for (int w = 0; w < kTopkWarps; ++w) {
+      a += warp_gt[w];
+      e += warp_eq[w];
+    }
+    cta_gt = a;
+    cta_eq = e;
+  }
+  cl.sync();   // every rank's counts are visible
   int gt_before = 0, eq_before = 0;
+  {
+    int g[kTopkRanks], e[kTopkRanks];
+#pragma unroll
+    for (int r = 0; r < kTopkRanks; ++r) {
+      g[r] = r < rank ? *cl.map_shared_rank(&cta_gt, r) : 0;
+      e[r] = r < rank ? *cl.map_shared_rank(&cta_eq, r) : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kTopkRanks; ++r) {
+      gt_before += g[r];
+      eq_before += e[r];
+    }
+  }
   for (int w = 0; w < warp; ++w) {
     gt_before += warp_gt[w];
     eq_before += warp_eq[w];
   }
   int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
   int eq_seen = eq_before;
-  for (int j0 = lo; j0 < hi; j0 += 32) {
+  for (int j0 = wlo; j0 < whi; j0 += 32) {
     const int j = j0 + lane;
-    const uint32_t key = j < hi ? key_at(j) : 0u;
-    const bool is_gt = j < hi && key > T, is_eq = j < hi && key == T;
+    const uint32_t key = j < whi ? key_at(j) : 0u;
+    const bool is_gt = j < whi && key > T, is_eq = j < whi && key == T;
     const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
     const bool take = is_gt || (is_eq && eq_seen + __popc(eqm & lt_mask) < need_eq);
     const unsigned tm = __ballot_sync(0xffffffffu, take);
@@ -179,39 +285,7 @@ __device__ __forceinline__ void select_request(int n4, int n_sel, const uint32_t
     pos += __popc(tm);
     eq_seen += __popc(eqm);
   }
-}
-
-__global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int n_sel,
-                                                             const int32_t* __restrict__ L,
-                                                             const float* __restrict__ score,
-                                                             int32_t* __restrict__ sel,
-                                                             int32_t* status) {
-  extern __shared__ __align__(16) uint32_t keys_smem[];
-  __shared__ unsigned hist[256];
-  __shared__ int warp_gt[32], warp_eq[32];
-  __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_krem;
-  const int b = blockIdx.x;
-  const int Lb = L[b];
-  const int64_t n4 = Lb >= 0 ? Lb / 4 : -1;
-  int32_t* out = sel + (int64_t)b * n_sel;
-  if (n4 < n_sel || n4 > c4_cap) {
-    if (threadIdx.x == 0) record_error(status, n4 > c4_cap ? TV_ERR_CAPACITY : TV_ERR_SELECTION);
-    for (int i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = -1;
-    return;
-  }
-  // n4 < 2^31: the shape check bounds B * c4_cap
-  const float* sc = score + (int64_t)b * c4_cap;
-  if (n4 <= kSmemKeys) {
-#pragma unroll 8
-    for (int j = threadIdx.x; j < (int)n4; j += blockDim.x) keys_smem[j] = score_key(sc[j]);
-    if (threadIdx.x < (unsigned)((-n4) & 3)) keys_smem[n4 + threadIdx.x] = 0u;   // whole vectors
-    select_request<true>((int)n4, n_sel, keys_smem, sc, out, hist, warp_gt, warp_eq, &s_prefix,
-                         &s_mask, &s_krem);
-  } else {
-    select_request<false>((int)n4, n_sel, keys_smem, sc, out, hist, warp_gt, warp_eq, &s_prefix,
-                          &s_mask, &s_krem);
-  }
+  cl.sync();   // no CTA leaves while a peer may still read its counts
 }
 
 }  // namespace
@@ -220,19 +294,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int64_t c4_cap, int
 int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const void* k_idx,
                       const int32_t* L, int32_t* sel, void* workspace, int32_t* status,
                       cudaStream_t stream) {
-  float* score = reinterpret_cast<float*>(workspace);
-  const int64_t n = (int64_t)s->B * s->c4_cap;
-  if (n > 0) {
-    tv::score_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
-        s->B, s->c4_cap, d_idx, reinterpret_cast<const uint16_t*>(q_idx),
-        reinterpret_cast<const uint16_t*>(k_idx), L, score);
-    if (int rc = tv_check_launch("tv_indexer_topk (scores)")) return rc;
-  }
-  // shared memory for the staged keys, sized by the capacity (requests with more entries than
-  // kSmemKeys read the scores from global memory instead)
-  // (rounded up to whole 16-byte vectors: the histogram passes read four keys at a time)
-  const int64_t staged = s->c4_cap < tv::kSmemKeys ? s->c4_cap : tv::kSmemKeys;
-  const size_t smem = (size_t)((staged + 3) / 4 * 4) * sizeof(uint32_t);
+  // shared memory for the staged keys, sized by the capacity (rounded up to whole 16-byte vectors)
+  const int64_t per = (s->c4_cap + tv::kTopkRanks - 1) / tv::kTopkRanks;
+  const int64_t staged = per <= tv::kStageKeys ? per : 0;
+  const size_t smem = tv::kKeyTiles * (size_t)tv::kKeyTileBytes +
+                      (size_t)((staged + 3) / 4 * 4) * sizeof(uint32_t);
   // once per device (a plain host call that also stays out of any stream being captured)
   static std::mutex attr_mu;
   static bool attr_set[64] = {};
@@ -242,13 +308,17 @@ int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const voi
   {
     std::lock_guard<std::mutex> lock(attr_mu);
     if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(tv::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(tv::kSmemKeys * sizeof(uint32_t))) != cudaSuccess)
+      if (cudaFuncSetAttribute(tv::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(tv::kKeyTiles * tv::kKeyTileBytes +
+                                     tv::kStageKeys * sizeof(uint32_t))) !=
+          cudaSuccess)
         return tv_check_launch("tv_indexer_topk (shared-memory attribute)");
       attr_set[dev] = true;
     }
   }
-  tv::select_kernel<<<s->B, tv::kSelThreads, smem, stream>>>(s->c4_cap, s->n_sel, L, score, sel,
-                                                             status);
-  return tv_check_launch("tv_indexer_topk (select)");
+  tv::topk_kernel<<<dim3(tv::kTopkRanks, s->B), tv::kTopkThreads, smem, stream>>>(
+      s->c4_cap, d_idx, s->n_sel, reinterpret_cast<const uint16_t*>(q_idx),
+      reinterpret_cast<const uint16_t*>(k_idx), L, reinterpret_cast<float*>(workspace), sel,
+      status);
+  return tv_check_launch("tv_indexer_topk");
 }
