@@ -795,17 +795,17 @@ def run_draft(args):
 
 def launches_per_step(shape, kernel):
     # plan, branch compress, accept, refresh + attention: SIMT (partials, merge; + the indexer's
-    # kernel on the sparse path) or tensor cores
+    # score and select kernels on the sparse path) or tensor cores
     # (selection gather when a C4 selection list is given, request ranking, pair kernel, merge
     # when the KV is split)
     from tree_speculative_verify_gb300 import _lib
     if kernel == "simt":
-        return 6 + (1 if shape.n_sel > 0 else 0)
+        return 6 + (2 if shape.n_sel > 0 else 0)
     gather = shape.B * shape.n_sel * 512 * 2 * 2
     split = _lib.tv_workspace_size(shape) > ((shape.B * 4 + 255) // 256) * 256 + gather
-    # + the indexer's top-k kernel and the selection gather on the sparse path, and the gather of
-    # the C128 entries and raw tails from page pools
-    return (4 + 2 + (1 if split else 0) + (2 if shape.n_sel > 0 else 0)
+    # + the indexer's score and select kernels and the selection gather on the sparse path, and
+    # the gather of the C128 entries and raw tails from page pools
+    return (4 + 2 + (1 if split else 0) + (3 if shape.n_sel > 0 else 0)
             + (1 if shape.page_tokens > 0 else 0))
 
 

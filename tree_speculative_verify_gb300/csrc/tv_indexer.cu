@@ -11,18 +11,21 @@
 // sum in index order i = 0 .. d_idx-1 with one round-to-nearest-even per addition and no fused
 // multiply-add (__fmul_rn / __fadd_rn).
 //
-// One kernel, a cluster of eight CTAs per request; CTA r owns the request's r-th contiguous eighth
-// of the C4 entries:
-//   1. scores of its entries -> order-preserving keys in shared memory, the indexer keys
-//      streamed through shared memory in contiguous tiles, several in flight, one thread per row;
+// Two kernels:
+//   1. score_kernel, over every SM: CTA (t, b) forms the scores of one tile of request b's C4
+//      entries from a coalesced copy of their indexer keys in shared memory (one thread per
+//      entry) and writes them to the workspace;
+//   select_kernel, a cluster of eight CTAs per request, CTA r owning the request's r-th contiguous
+//   eighth of the entries (their order-preserving keys staged in shared memory):
 //   2. an 8-bit-digit radix select of the n_sel-th largest key over the whole request: per pass
 //      every CTA counts its keys into a shared-memory histogram, and after one cluster barrier each
 //      CTA sums the eight histograms through distributed shared memory and picks the same digit;
 //   3. the kept entries in ascending order: every warp counts the entries above the threshold and
 //      the ties in its contiguous index range, CTAs in rank order and warps in index order place
 //      them (ties: the lowest indices), and each warp writes its own.
+//   The select kernel is a programmatic dependent of the score kernel: its launch overlaps the
+//   scoring, and it waits for the scores before it reads them.
 #include <cooperative_groups.h>
-#include <mutex>
 
 #include "tv_common.cuh"
 
@@ -32,21 +35,20 @@ namespace {
 constexpr int kTopkRanks = 8;        // CTAs per request (one cluster)
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
-// Keys a CTA stages in shared memory (24 KB, beside three 64 KB key tiles and the static arrays):
-// its share of a request of up to 8 x 6144 C4 entries.  A larger share keeps its scores in the
-// workspace and re-reads them in each pass.
+// Keys a select CTA stages in shared memory (24 KB): its share of a request of up to 8 x 6144 C4
+// entries.  A larger share reads its scores from the workspace in each pass.
 constexpr int kStageKeys = 6144;
-constexpr int kMaxIdxVec = 64;       // 16-byte vectors of the indexer query (d_idx <= 512)
-constexpr int kKeyTileBytes = 65536; // indexer keys staged per tile
-constexpr int kKeyTiles = 3;         // tiles in flight
+constexpr int kMaxIdxVec = 32;       // 16-byte vectors of the indexer query (d_idx <= 256)
+constexpr int kScoreThreads = 256;
+constexpr int kScoreTileBytes = 32768;   // indexer keys of one score CTA
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_two() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_none() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 
 // Order-preserving map of an fp32 score to an unsigned key (larger score -> larger key); -0 and
 // +0 map to the same key.
@@ -59,19 +61,61 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// grid (8, B), clusters of 8 along x.  score_ws: [B][c4_cap] fp32, used only when a CTA's share
-// exceeds kStageKeys.
+// Rows per score CTA: kScoreTileBytes of indexer keys of dimension d_idx = 8 nvec.
+__host__ __device__ __forceinline__ int score_rows(int nvec) { return kScoreTileBytes / (16 * nvec); }
+
+// grid (ceil(c4_cap / score_rows), B).  CTA (t, b) scores entries t RT .. t RT + RT - 1 of request
+// b (those below L[b] / 4) into score_ws[b][j].  A request whose L is negative or past the
+// capacity is skipped (the select kernel reports it).
+__global__ void __launch_bounds__(kScoreThreads, 4)
+    score_kernel(int64_t c4_cap, int d_idx, const uint16_t* __restrict__ q_idx,
+                 const uint16_t* __restrict__ k_idx, const int32_t* __restrict__ L,
+                 float* __restrict__ score_ws) {
+  pdl_launch_dependents();   // the select kernel may be placed; it waits for these scores
+  __shared__ uint4 ktile[kScoreTileBytes / 16];
+  __shared__ uint4 q[kMaxIdxVec];
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const int nvec = d_idx / 8, RT = score_rows(nvec);
+  const int64_t n4 = L[b] >= 0 ? L[b] / 4 : -1;
+  const int64_t j0 = (int64_t)blockIdx.x * RT;
+  if (n4 < 0 || n4 > c4_cap || j0 >= n4) return;
+  const int rows = (int)(n4 - j0 < RT ? n4 - j0 : RT);
+  // the tile's rows as contiguous 16-byte chunks; chunk c of row r sits at r * nvec + (c ^ (r & 7))
+  // when nvec is a multiple of 8, so the threads' row-wise reads do not collide on banks
+  const int swz = (nvec & 7) == 0 ? 7 : 0;
+  const uint4* src = reinterpret_cast<const uint4*>(k_idx + ((int64_t)b * c4_cap + j0) * d_idx);
+  for (int i = tid; i < rows * nvec; i += blockDim.x) {
+    const int r = i / nvec, c = i - r * nvec;
+    cp_async16(ktile + r * nvec + (c ^ (r & swz)), src + i);
+  }
+  if (tid < nvec) q[tid] = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx)[tid];
+  cp_async_wait_all();
+  __syncthreads();
+  float* sc = score_ws + (int64_t)b * c4_cap + j0;
+  for (int r = tid; r < rows; r += blockDim.x) {
+    float sacc = 0.f;
+    for (int c = 0; c < nvec; ++c) {
+      const uint4 qa = q[c], ka = ktile[r * nvec + (c ^ (r & swz))];
+      const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {   // element 2h (low half) before 2h+1 (high half)
+        sacc = __fadd_rn(sacc, __fmul_rn(bf16_lo(qw[h]), bf16_lo(kw[h])));
+        sacc = __fadd_rn(sacc, __fmul_rn(bf16_hi(qw[h]), bf16_hi(kw[h])));
+      }
+    }
+    sc[r] = sacc;
+  }
+}
+
+// grid (8, B), clusters of 8 along x; launched as a programmatic dependent of score_kernel.
+// score_ws: [B][c4_cap] fp32 scores.
 __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThreads)
-    topk_kernel(int64_t c4_cap, int d_idx, int n_sel, const uint16_t* __restrict__ q_idx,
-                const uint16_t* __restrict__ k_idx, const int32_t* __restrict__ L,
-                float* __restrict__ score_ws, int32_t* __restrict__ sel, int32_t* status) {
+    select_kernel(int64_t c4_cap, int n_sel, const int32_t* __restrict__ L,
+                  const float* __restrict__ score_ws, int32_t* __restrict__ sel,
+                  int32_t* status) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
-  extern __shared__ __align__(16) uint32_t smem_dyn[];
-  // kKeyTiles tiles of indexer keys in flight, then this CTA's keys (when staged)
-  uint4* ktile = reinterpret_cast<uint4*>(smem_dyn);
-  uint32_t* keys = smem_dyn + kKeyTiles * kKeyTileBytes / 4;
-  __shared__ uint4 q[kMaxIdxVec];
+  extern __shared__ __align__(16) uint32_t keys[];   // this CTA's keys (when staged)
   __shared__ unsigned hist[2][256];   // by pass parity (a rank that runs ahead never clears a
                                       // histogram a slower rank still reads)
   __shared__ unsigned ghist[256];     // the pass's histogram of the whole request
@@ -79,6 +123,7 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
   __shared__ int cta_gt, cta_eq;
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_krem;
+  pdl_wait();   // the scores are complete and visible
   const int b = blockIdx.y;
   const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -97,65 +142,17 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
   const int per = (n4 + kTopkRanks - 1) / kTopkRanks;
   const int lo = min(n4, rank * per), hi = min(n4, lo + per), n = hi - lo;
   const bool staged = per <= kStageKeys;   // uniform over the cluster
-  float* sc = score_ws + (int64_t)b * c4_cap;
-  const int nvec = d_idx / 8;
-  // 1. scores of this CTA's entries -> keys
-  if (tid < nvec) q[tid] = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx)[tid];
+  const float* sc = score_ws + (int64_t)b * c4_cap;
   if (tid == 0) {
     s_prefix = 0u;
     s_mask = 0u;
     s_krem = n_sel;
   }
-  __syncthreads();
-  // the CTA's indexer keys stream through shared memory in tiles of RT rows, read as contiguous
-  // 16-byte chunks (kKeyTiles tiles in flight); chunk c of row r sits at r * nvec + (c ^ (r & 7)) when
-  // nvec is a multiple of 8, so the threads' row-wise reads do not collide on banks; thread r then
-  // forms row r's score with the (strictly ordered) additions
-  const int RT = kKeyTileBytes / (16 * nvec);
-  const int swz = (nvec & 7) == 0 ? 7 : 0;
-  const uint4* kbase = reinterpret_cast<const uint4*>(k_idx + ((int64_t)b * c4_cap + lo) * d_idx);
-  const int n_tiles = (n + RT - 1) / RT;
-  auto issue = [&](int tile) {
-    if (tile < n_tiles) {
-      uint4* dst = ktile + (tile % kKeyTiles) * (kKeyTileBytes / 16);
-      const int rows = min(RT, n - tile * RT);
-      const uint4* src = kbase + (int64_t)tile * RT * nvec;
-      for (int i = tid; i < rows * nvec; i += blockDim.x) {
-        const int r = i / nvec, c = i - r * nvec;
-        cp_async16(dst + r * nvec + (c ^ (r & swz)), src + i);
-      }
-    }
-    cp_async_commit();
-  };
-  issue(0);
-  issue(1);
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    issue(tile + 2);
-    cp_async_wait_two();   // this tile's copies have landed; the next two may be in flight
-    __syncthreads();
-    const uint4* kt = ktile + (tile % kKeyTiles) * (kKeyTileBytes / 16);
-    const int rows = min(RT, n - tile * RT);
-    for (int r = tid; r < rows; r += blockDim.x) {
-      float sacc = 0.f;
-      for (int c = 0; c < nvec; ++c) {
-        const uint4 qa = q[c], ka = kt[r * nvec + (c ^ (r & swz))];
-        const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {   // element 2h (low half) before 2h+1 (high half)
-          sacc = __fadd_rn(sacc, __fmul_rn(bf16_lo(qw[h]), bf16_lo(kw[h])));
-          sacc = __fadd_rn(sacc, __fmul_rn(bf16_hi(qw[h]), bf16_hi(kw[h])));
-        }
-      }
-      const int j = lo + tile * RT + r;
-      if (staged)
-        keys[j - lo] = score_key(sacc);
-      else
-        sc[j] = sacc;
-    }
-    __syncthreads();   // the tile's buffer may be refilled
+  // 1. this CTA's keys (the padding up to whole 16-byte vectors: key 0, never counted)
+  if (staged) {
+    for (int j = lo + tid; j < hi; j += blockDim.x) keys[j - lo] = score_key(sc[j]);
+    if (tid < ((-n) & 3)) keys[n + tid] = 0u;
   }
-  cp_async_wait_none();
-  if (staged && tid < ((-n) & 3)) keys[n + tid] = 0u;   // whole 16-byte vectors
   __syncthreads();
   auto key_at = [&](int j) -> uint32_t { return staged ? keys[j - lo] : score_key(sc[j]); };
   // 2. radix select of the n_sel-th largest key of the request, most significant digit first
@@ -294,31 +291,21 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
 int tv_launch_indexer(const tv_shape* s, int d_idx, const void* q_idx, const void* k_idx,
                       const int32_t* L, int32_t* sel, void* workspace, int32_t* status,
                       cudaStream_t stream) {
+  float* score_ws = reinterpret_cast<float*>(workspace);
+  const int RT = tv::score_rows(d_idx / 8);
+  const int64_t tiles = (s->c4_cap + RT - 1) / RT;
+  if (tiles > 0) {
+    tv::score_kernel<<<dim3((unsigned)tiles, s->B), tv::kScoreThreads, 0, stream>>>(
+        s->c4_cap, d_idx, reinterpret_cast<const uint16_t*>(q_idx),
+        reinterpret_cast<const uint16_t*>(k_idx), L, score_ws);
+    if (int rc = tv_check_launch("tv_indexer_topk (scores)")) return rc;
+  }
   // shared memory for the staged keys, sized by the capacity (rounded up to whole 16-byte vectors)
   const int64_t per = (s->c4_cap + tv::kTopkRanks - 1) / tv::kTopkRanks;
   const int64_t staged = per <= tv::kStageKeys ? per : 0;
-  const size_t smem = tv::kKeyTiles * (size_t)tv::kKeyTileBytes +
-                      (size_t)((staged + 3) / 4 * 4) * sizeof(uint32_t);
-  // once per device (a plain host call that also stays out of any stream being captured)
-  static std::mutex attr_mu;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-    return tv_check_launch("tv_indexer_topk (device query)");
-  {
-    std::lock_guard<std::mutex> lock(attr_mu);
-    if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(tv::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(tv::kKeyTiles * tv::kKeyTileBytes +
-                                     tv::kStageKeys * sizeof(uint32_t))) !=
-          cudaSuccess)
-        return tv_check_launch("tv_indexer_topk (shared-memory attribute)");
-      attr_set[dev] = true;
-    }
-  }
-  tv::topk_kernel<<<dim3(tv::kTopkRanks, s->B), tv::kTopkThreads, smem, stream>>>(
-      s->c4_cap, d_idx, s->n_sel, reinterpret_cast<const uint16_t*>(q_idx),
-      reinterpret_cast<const uint16_t*>(k_idx), L, reinterpret_cast<float*>(workspace), sel,
-      status);
+  const size_t smem = (size_t)((staged + 3) / 4 * 4) * sizeof(uint32_t);
+  tv::launch_pdl(tv::select_kernel, dim3(tv::kTopkRanks, s->B), dim3(tv::kTopkThreads), smem,
+                 stream, (int64_t)s->c4_cap, (int)s->n_sel, L, (const float*)score_ws, sel,
+                 status);
   return tv_check_launch("tv_indexer_topk");
 }
