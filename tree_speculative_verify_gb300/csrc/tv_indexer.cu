@@ -9,7 +9,7 @@
 // Precision: the scores decide an integer selection, so the kernel fixes them exactly: bf16
 // inputs; each product rounded to fp32 (exact for bf16 operands) and added to the running fp32
 // sum in index order i = 0 .. d_idx-1 with one round-to-nearest-even per addition and no fused
-// multiply-add (__fmul_rn / __fadd_rn).
+// multiply-add (products by round-to-nearest packed fp32 multiplies, sums by __fadd_rn).
 //
 // Two kernels:
 //   1. score_kernel, over every SM: CTA (t, b) forms the scores of one tile of request b's C4
@@ -61,6 +61,16 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// The products a0 b0 and a1 b1 by one packed fp32 multiply, each rounded to nearest (as __fmul_rn).
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& p0,
+                                        float& p1) {
+  uint64_t a, b, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(p0), "=f"(p1) : "l"(d));
+}
+
 // Rows per score CTA: kScoreTileBytes of indexer keys of dimension d_idx = 8 nvec.
 __host__ __device__ __forceinline__ int score_rows(int nvec) { return kScoreTileBytes / (16 * nvec); }
 
@@ -73,7 +83,7 @@ __global__ void __launch_bounds__(kScoreThreads, 4)
                  float* __restrict__ score_ws) {
   pdl_launch_dependents();   // the select kernel may be placed; it waits for these scores
   __shared__ uint4 ktile[kScoreTileBytes / 16];
-  __shared__ uint4 q[kMaxIdxVec];
+  __shared__ float4 qf[2 * kMaxIdxVec];   // the query in fp32 (exact)
   const int b = blockIdx.y, tid = threadIdx.x;
   const int nvec = d_idx / 8, RT = score_rows(nvec);
   const int64_t n4 = L[b] >= 0 ? L[b] / 4 : -1;
@@ -88,19 +98,27 @@ __global__ void __launch_bounds__(kScoreThreads, 4)
     const int r = i / nvec, c = i - r * nvec;
     cp_async16(ktile + r * nvec + (c ^ (r & swz)), src + i);
   }
-  if (tid < nvec) q[tid] = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx)[tid];
+  if (tid < nvec) {
+    const uint4 qa = reinterpret_cast<const uint4*>(q_idx + (int64_t)b * d_idx)[tid];
+    qf[2 * tid] = make_float4(bf16_lo(qa.x), bf16_hi(qa.x), bf16_lo(qa.y), bf16_hi(qa.y));
+    qf[2 * tid + 1] = make_float4(bf16_lo(qa.z), bf16_hi(qa.z), bf16_lo(qa.w), bf16_hi(qa.w));
+  }
   cp_async_wait_all();
   __syncthreads();
   float* sc = score_ws + (int64_t)b * c4_cap + j0;
   for (int r = tid; r < rows; r += blockDim.x) {
     float sacc = 0.f;
     for (int c = 0; c < nvec; ++c) {
-      const uint4 qa = q[c], ka = ktile[r * nvec + (c ^ (r & swz))];
-      const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+      const uint4 ka = ktile[r * nvec + (c ^ (r & swz))];
+      const float4 qa = qf[2 * c], qb = qf[2 * c + 1];
+      const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+      const uint32_t kw[4] = {ka.x, ka.y, ka.z, ka.w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {   // element 2h (low half) before 2h+1 (high half)
-        sacc = __fadd_rn(sacc, __fmul_rn(bf16_lo(qw[h]), bf16_lo(kw[h])));
-        sacc = __fadd_rn(sacc, __fmul_rn(bf16_hi(qw[h]), bf16_hi(kw[h])));
+        float p0, p1;
+        mul2_rn(qv[2 * h], qv[2 * h + 1], bf16_lo(kw[h]), bf16_hi(kw[h]), p0, p1);
+        sacc = __fadd_rn(sacc, p0);
+        sacc = __fadd_rn(sacc, p1);
       }
     }
     sc[r] = sacc;
@@ -149,8 +167,19 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
     s_krem = n_sel;
   }
   // 1. this CTA's keys (the padding up to whole 16-byte vectors: key 0, never counted)
-  if (staged) {
-    for (int j = lo + tid; j < hi; j += blockDim.x) keys[j - lo] = score_key(sc[j]);
+  if (staged) {   // all of a thread's loads in flight at once
+    constexpr int kPerThread = (kStageKeys + kTopkThreads - 1) / kTopkThreads;
+    float v[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int j = lo + tid + k * kTopkThreads;
+      v[k] = j < hi ? sc[j] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int j = lo + tid + k * kTopkThreads;
+      if (j < hi) keys[j - lo] = score_key(v[k]);
+    }
     if (tid < ((-n) & 3)) keys[n + tid] = 0u;
   }
   __syncthreads();
