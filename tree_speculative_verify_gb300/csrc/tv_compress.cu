@@ -237,10 +237,12 @@ __device__ void entry4(int d, const float* gate, T* outK, T* outV, T* out2K, T* 
 // the rescaled sum of weights.  All orders are fixed: the entry depends only on the block's rows,
 // so prefill and the scratch pad agree bit for bit.  parity: the entry's index & 1 among the
 // cluster's consecutive entries (the receive buffers alternate, so a rank that runs ahead into
-// the next entry never writes a buffer that a slower rank still reads).
-template <typename T>
-__device__ void entry128(int d, const float* gate, T* outK, T* outV, int parity,
-                         C128Smem<T>& sm) {
+// the next entry never writes a buffer that a slower rank still reads).  after_rows() runs on
+// every thread once the rank's sums are sent, before the cluster barrier: the caller may refetch
+// rows there (after a barrier of its own, since other threads may still read them).
+template <typename T, typename AfterRows>
+__device__ void entry128(int d, const float* gate, T* outK, T* outV, int parity, C128Smem<T>& sm,
+                         AfterRows&& after_rows) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -270,6 +272,7 @@ __device__ void entry128(int d, const float* gate, T* outK, T* outV, int parity,
     for (int t = 0; t < kC128Tokens; ++t) s += sm.w[t];
     *cl.map_shared_rank(&sm.ms[parity][rank], (int)threadIdx.x) = make_float2(m, s);
   }
+  after_rows();
   cl.sync();   // every rank's sums have arrived
   pdl_wait();   // (scratch pad) the kernel before this one has completed before any store
   const int p = rank * ppr + (int)threadIdx.x;
@@ -360,7 +363,7 @@ __global__ void __cluster_dims__(kC128Ranks, 1, 1) __launch_bounds__(kThreads)
     fetch_rows<T>(sm.rows, rowK, rowV, kC128Tokens, nullptr, d);
     cp_async_commit();
     const int64_t out = layer_row(pg, b, j, cap_m, 128, status) * d;
-    entry128<T>(d, sm.gate128, CK + out, CV + out, parity, sm);
+    entry128<T>(d, sm.gate128, CK + out, CV + out, parity, sm, [] {});
   }
 }
 
@@ -488,6 +491,7 @@ __global__ void __cluster_dims__(kC128Ranks, 1, 1) __launch_bounds__(kThreads)
   __shared__ const T* rowK[kC128Tokens];
   __shared__ const T* rowV[kC128Tokens];
   __shared__ bool tree_tok[kC128Tokens];   // this CTA's C128 token is a tree row
+  __shared__ int s_any_tree;               // some token of this CTA is a tree row
   __shared__ int path[kMaxD];              // path of the C128 entry in progress
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
@@ -535,9 +539,13 @@ __global__ void __cluster_dims__(kC128Ranks, 1, 1) __launch_bounds__(kThreads)
     c4_rows(pg, b, D, d, raw_cap, Lb, s_list4[rank], s_dep, s_par, rawK, rawV, treeK, treeV,
             tid - 32, rowK4, rowV4, status);
   __syncthreads();
-  if (n128 > 0 && tid < kC128Tokens)
+  if (tid == 0) s_any_tree = 0;
+  __syncthreads();
+  if (n128 > 0 && tid < kC128Tokens) {
     tree_tok[tid] = c128_row(pg, b, D, d, raw_cap, Lb, pos128, rank, path, rawK, rawV, treeK,
                              treeV, tid, rowK, rowV, status);
+    if (tree_tok[tid]) s_any_tree = 1;
+  }
   __syncthreads();
   if (rank < n4) {
     fetch_rows<T>(sm.c4.rows4, rowK4, rowV4, 4, nullptr, d);
@@ -598,21 +606,25 @@ __global__ void __cluster_dims__(kC128Ranks, 1, 1) __launch_bounds__(kThreads)
               sm.c4);
   }
   // 6. C128 entries, one after another by the whole cluster (uniform over the cluster); the
-  //    block's committed rows stay in place, only the tree rows change between entries
+  //    block's committed rows stay in place, only the tree rows change between entries: a CTA
+  //    holding tree rows fetches the next entry's as soon as its sums for this one are sent
+  const bool any_tree = s_any_tree != 0;   // uniform over the CTA
   for (int j = 0; j < n128; ++j) {
     const int v = s_list128[j];
-    if (j > 0) {
-      if (tid == 0) c128_path(v);
-      __syncthreads();
-      if (tid < kC128Tokens && tree_tok[tid])
-        c128_row(pg, b, D, d, raw_cap, Lb, pos128, rank, path, rawK, rawV, treeK, treeV, tid,
-                 rowK, rowV, status);
-      __syncthreads();
-      fetch_rows<T>(sm.c128.rows, rowK, rowV, kC128Tokens, tree_tok, d);
-      cp_async_commit();
-    }
     const int64_t out = ((int64_t)b * D + v) * d;
-    entry128<T>(d, sm.c128.gate128, scrK128 + out, scrV128 + out, j & 1, sm.c128);
+    entry128<T>(d, sm.c128.gate128, scrK128 + out, scrV128 + out, j & 1, sm.c128, [&] {
+      if (j + 1 < n128 && any_tree) {
+        __syncthreads();   // every thread is done with this entry's rows
+        if (tid == 0) c128_path(s_list128[j + 1]);
+        __syncthreads();
+        if (tid < kC128Tokens && tree_tok[tid])
+          c128_row(pg, b, D, d, raw_cap, Lb, pos128, rank, path, rawK, rawV, treeK, treeV, tid,
+                   rowK, rowV, status);
+        __syncthreads();
+        fetch_rows<T>(sm.c128.rows, rowK, rowV, kC128Tokens, tree_tok, d);
+        cp_async_commit();
+      }
+    });
   }
 }
 
@@ -729,13 +741,31 @@ __global__ void refresh_kernel(Paging pg, int D, int d, int es, int comp_mask, i
     }
   }
   __syncthreads();
+  // the copies, kCopyUnroll chunks per thread with all their loads in flight before the stores
+  constexpr int kCopyUnroll = 4;
   const int chunks = (int)(row_bytes / 16);
   const int total = 3 * n * chunks;
-  for (int k = tid; k < total; k += blockDim.x) {
-    const int j = k / chunks, c = k - j * chunks;
-    if (s_srcK[j] == nullptr) continue;
-    reinterpret_cast<uint4*>(s_dstK[j])[c] = reinterpret_cast<const uint4*>(s_srcK[j])[c];
-    reinterpret_cast<uint4*>(s_dstV[j])[c] = reinterpret_cast<const uint4*>(s_srcV[j])[c];
+  for (int k0 = tid; k0 < total; k0 += kCopyUnroll * blockDim.x) {
+    uint4 vk[kCopyUnroll], vv[kCopyUnroll];
+    int jc[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int k = k0 + u * blockDim.x;
+      const int j = k / chunks, c = k - j * chunks;
+      jc[u] = -1;
+      if (k < total && s_srcK[j] != nullptr) {
+        vk[u] = reinterpret_cast<const uint4*>(s_srcK[j])[c];
+        vv[u] = reinterpret_cast<const uint4*>(s_srcV[j])[c];
+        jc[u] = k;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      if (jc[u] < 0) continue;
+      const int j = jc[u] / chunks, c = jc[u] - j * chunks;
+      reinterpret_cast<uint4*>(s_dstK[j])[c] = vk[u];
+      reinterpret_cast<uint4*>(s_dstV[j])[c] = vv[u];
+    }
   }
   for (int i = tid; i < D; i += blockDim.x) cpos[i] = i < n ? Lb + i : -1;
   __syncthreads();
