@@ -51,8 +51,16 @@
 // TMEM columns: pair S: S buffers at [0,128) and [128,256), Q at [256,512); pair O: O at [0,512).
 // Every wait is bounded; on timeout the CTA records TV_ERR_TIMEOUT, sets the abort flag of all
 // four CTAs, stops issuing work, drains its own copies and MMAs (bounded) and frees its TMEM.
-// The kernel is a programmatic dependent of the scheduling kernel: its set-up (barriers, TMEM,
-// tensor-map prefetch) overlaps that kernel, and it reads the round's inputs only after it.
+// Launch chain.  On the contiguous dense path with up to kRankMax requests the kernel is a
+// programmatic dependent of the kernel before it in the stream (in a round: the scratch pad) and
+// ranks the requests itself in its prologue (from the lengths L, which that kernel does not
+// write): it streams the prefix tiles while the scratch pad still runs, and waits for that
+// kernel only where it reads what the round's earlier kernels wrote -- the softmax warps before
+// the plan's masks (at the first item's first raw or extra tile; later items read them at their
+// start), the producer before the scratch rows (the extra tile, each item's last), every thread
+// before a global write -- and before it exits, so that its completion still implies theirs.  The lengths are read once, in
+// the prologue, through L2.  Otherwise (larger batches, selection lists, page pools) the
+// requests are ranked by order_kernel, which this kernel waits for before it starts.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -84,6 +92,16 @@ constexpr int kPMsg = kPBytes + 128 * 4;   // P and the rows' rescale factors, s
 constexpr int kPBuf = 33 * 1024;           // a P buffer (1 KB aligned)
 constexpr int kDp = 8;          // rows per section of the extra tile (D <= 8)
 constexpr int kExtraEntries = 32;   // tree | C4 scratch | C128 scratch | zeros
+constexpr int kRankMax = 2048;      // batches up to this size are ranked in the kernel's prologue
+
+// The wait for the kernel this one depends on, at most once per thread (waited: this thread has
+// waited, or the whole CTA did in the prologue); a repeated griddepcontrol.wait is not free.
+__device__ __forceinline__ void pdl_wait_once(bool& waited) {
+  if (!waited) {
+    pdl_wait();
+    waited = true;
+  }
+}
 constexpr uint32_t kTmemQ = 256;     // pair S: Q columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // default bound of every wait
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P values stay below 2^8
@@ -125,9 +143,8 @@ struct Tile {
   int kind, row0, valid, nqk;
 };
 
-__device__ __forceinline__ Layout layout_of(const Params& p, int b) {
+__device__ __forceinline__ Layout layout_for(const Params& p, int L) {
   Layout y;
-  const int L = p.L[b];
   const bool c4 = p.comp_mask & TV_COMP_C4, c128 = p.comp_mask & TV_COMP_C128;
   const int n4 = c4 ? (p.n_sel > 0 ? p.n_sel : L / 4) : 0;
   const bool ok = L >= 0 && L <= p.raw_cap && n4 <= p.c4_cap && (!c128 || L / 128 <= p.c128_cap);
@@ -147,6 +164,7 @@ __device__ __forceinline__ Layout layout_of(const Params& p, int b) {
   y.T = y.T4 + y.T128 + y.Traw + 1;
   return y;
 }
+__device__ __forceinline__ Layout layout_of(const Params& p, int b) { return layout_for(p, p.L[b]); }
 
 __device__ __forceinline__ Tile tile_of(const Layout& y, int t) {
   Tile x;
@@ -301,6 +319,9 @@ struct Header {
   int xok_end[2][4];           // pair S: [column half][lane quadrant] carries on after an item
   uint32_t tmem;
   int abort;
+  int32_t len[kRankMax];       // the requests' lengths L (read once, in the prologue)
+  uint16_t order[kRankMax];    // requests by decreasing tile count (ranked in the prologue)
+  uint16_t tiles[kRankMax];    // tile counts of the requests (clamped to 65535; ranking only)
 };
 // A P buffer holds 128 rows x 128 entries of bf16 P as two 64-entry panels (K-major, 128-byte
 // swizzle), followed by the 128 rows' fp32 rescale factors.
@@ -415,7 +436,8 @@ struct Item {
   Layout y;
 };
 
-__device__ __forceinline__ bool item_at(const Params& p, int k, uint32_t sub, Item& it) {
+__device__ __forceinline__ bool item_at(const Params& p, const Smem& sm, int k, uint32_t sub,
+                                        Item& it) {
   const int G = (int)(gridDim.x / kClusterCtas), c = (int)(blockIdx.x / kClusterCtas);
   const int pos = (k & 1) ? k * G + (G - 1 - c) : k * G + c;
   if (pos >= p.B * p.n_chunks * p.n_pairs) return false;
@@ -423,9 +445,14 @@ __device__ __forceinline__ bool item_at(const Params& p, int k, uint32_t sub, It
   const int pair_idx = x % p.n_pairs;
   x /= p.n_pairs;
   it.chunk = x % p.n_chunks;
-  it.b = p.order[x / p.n_chunks];
+  if (p.order != nullptr) {
+    it.b = p.order[x / p.n_chunks];
+    it.y = layout_of(p, it.b);
+  } else {
+    it.b = sm.h.order[x / p.n_chunks];
+    it.y = layout_for(p, sm.h.len[it.b]);
+  }
   it.rt = 2 * pair_idx + (int)sub;
-  it.y = layout_of(p, it.b);
   if (it.y.T == 0) {   // capacity exceeded: nothing is computed for this request
     it.tb = it.te = 0;
     if (threadIdx.x == 0) record_error(p.status, TV_ERR_CAPACITY);
@@ -457,10 +484,11 @@ struct Ring {
 // slices.  Pair O: every entry of each tile for this CTA's 256 value columns, in two slots (one
 // per 256-column group of O) of two 64-column blocks; rows past the tile's entry count rounded up
 // to 64 are not loaded.
-template <bool kPaged>
+template <bool kPaged, bool kOverlap>
 __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
   const int lane = threadIdx.x & 31;
   const uint32_t leader = cluster_rank() & ~1u;
+  bool waited = !kOverlap;   // (without the overlap the prologue waited)
   Ring r{role_s ? sm.buf : sm.buf + 2 * kPBuf, role_s ? kSSlots : kOSlots, 0, 0};
   bool issued[kSSlots];
   uint32_t issued_phase[kSSlots];
@@ -488,7 +516,7 @@ __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
   bool ok = true;
   int q = 0;   // non-empty items so far
   Item it;
-  for (int k = 0; ok && item_at(p, k, sub, it); ++k) {
+  for (int k = 0; ok && item_at(p, sm, k, sub, it); ++k) {
     if (it.tb >= it.te) continue;
     const int b = it.b;
     const Layout& y = it.y;
@@ -535,6 +563,7 @@ __device__ void producer(const Params& p, Smem& sm, bool role_s, uint32_t sub) {
     for (int t = it.tb; t < it.te && ok; ++t) {
       const int2 next = row_of(t + 1);
       const Tile x = tile_of(y, t);
+      if (kOverlap && x.kind == kExtra) pdl_wait_once(waited);   // the scratch rows
       for (int g = 0; g < 2 && ok; ++g) {
         if (!acquire()) {
           ok = false;
@@ -636,7 +665,7 @@ __device__ void mma_s(const Params& p, Smem& sm) {
   int g = 0, q = 0;   // tiles and non-empty items so far
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at(p, k, 0, it); ++k) {
+  for (int k = 0; ok && item_at(p, sm, k, 0, it); ++k) {
     const int n = it.te - it.tb;
     if (n <= 0) continue;
     if (!mbar_wait(&sm.h.q_full, q & 1, &sm.h.abort, p.timeout_ns)) {
@@ -698,7 +727,7 @@ __device__ void mma_o(const Params& p, Smem& sm) {
   int g = 0, q = 0;
   bool ok = true;
   Item it;
-  for (int k = 0; ok && item_at(p, k, 0, it); ++k) {
+  for (int k = 0; ok && item_at(p, sm, k, 0, it); ++k) {
     const int n = it.te - it.tb;
     if (n <= 0) continue;
     if (q > 0 && !mbar_wait(&sm.h.o_free, (q - 1) & 1, &sm.h.abort, p.timeout_ns)) {
@@ -769,7 +798,7 @@ __device__ void signal_s(const Params& p, Smem& sm, uint32_t rank) {
   const uint32_t src0 = smem_u32(sm.buf + kSSlots * kSlotBytes);
   int g = 0, q = 0;
   Item it;
-  for (int k = 0; item_at(p, k, rank & 1u, it); ++k) {
+  for (int k = 0; item_at(p, sm, k, rank & 1u, it); ++k) {
     const int n = it.te - it.tb;
     if (n <= 0) continue;
     if (!mbar_wait(&sm.h.q_local, q & 1, &sm.h.abort, p.timeout_ns)) {
@@ -817,7 +846,7 @@ __device__ void signal_o(const Params& p, Smem& sm, uint32_t rank) {
   const bool is_leader = (rank & 1u) == 0;
   int g = 0;
   Item it;
-  for (int k = 0; item_at(p, k, rank & 1u, it); ++k) {
+  for (int k = 0; item_at(p, sm, k, rank & 1u, it); ++k) {
     const int n = it.te - it.tb;
     bool ok = true;
     for (int i = 0; i < n; ++i, ++g) {
@@ -843,6 +872,32 @@ __device__ __forceinline__ void pair_sync(int quad) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
 }
 
+// The plan's visibility of one query row: (raw_lo << 32) | extra-tile mask (bit j: entry j of
+// the extra tile is visible); 0 for a row past D*H (grow < 0).  With wait, first the wait for the
+// kernel this one depends on (the plan's results come from an earlier kernel).  Not inlined: it
+// stays out of the softmax's tile loop.
+__device__ __noinline__ uint64_t row_masks(const Params& p, int b, int grow, int L, bool wait) {
+  if (wait) pdl_wait();
+  if (grow < 0) return 0;
+  const int v = grow / p.H;
+  const int64_t i = (int64_t)b * p.D + v;
+  const uint64_t an = p.anc[i];
+  const int raw_lo = p.raw_lo[i];
+  const uint64_t v4 = (p.comp_mask & TV_COMP_C4) ? p.vis4[i] : 0;
+  const uint64_t v128 = (p.comp_mask & TV_COMP_C128) ? p.vis128[i] : 0;
+  uint32_t extra_mask = 0;
+  for (int u = 0; u < p.D; ++u) {
+    if ((an >> u) & 1ull) {
+      const int dep = __popcll(an & ((1ull << u) - 1ull));
+      if (L + dep >= raw_lo) extra_mask |= 1u << u;
+    }
+    if ((v4 >> u) & 1ull) extra_mask |= 1u << (kDp + u);
+    if ((v128 >> u) & 1ull) extra_mask |= 1u << (2 * kDp + u);
+  }
+  return ((uint64_t)(uint32_t)raw_lo << 32) | extra_mask;
+}
+
+template <bool kOverlap>
 __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -859,8 +914,9 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
                           (row & 7) * 128;
   int g = 0, q = 0;
   bool ok = true;
+  bool waited = !kOverlap;   // this thread has waited for the kernel it depends on
   Item it;
-  for (int k = 0; ok && item_at(p, k, rank & 1u, it); ++k) {
+  for (int k = 0; ok && item_at(p, sm, k, rank & 1u, it); ++k) {
     const int n = it.te - it.tb;
     if (n <= 0) continue;
     const int b = it.b;
@@ -899,25 +955,20 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
     if (lane == 0 && ok) mbar_arrive(&sm.h.q_local);
     ++q;
 
-    // per-row visibility of the raw tail and of the extra tile
+    // per-row visibility of the raw tail and of the extra tile, from the plan's masks; read at
+    // the item's first raw or extra tile, after the wait for the round's earlier kernels (the
+    // prefix tiles before it need no mask); at the item's start once this thread has waited
     int raw_lo = 0;
     uint32_t extra_mask = 0;   // bit j: entry j of the extra tile is visible
-    if (row_ok) {
-      const int v = grow / p.H;
-      const int64_t i = (int64_t)b * p.D + v;
-      const uint64_t an = p.anc[i];
-      raw_lo = p.raw_lo[i];
-      const uint64_t v4 = (p.comp_mask & TV_COMP_C4) ? p.vis4[i] : 0;
-      const uint64_t v128 = (p.comp_mask & TV_COMP_C128) ? p.vis128[i] : 0;
-      for (int u = 0; u < p.D; ++u) {
-        if ((an >> u) & 1ull) {
-          const int dep = __popcll(an & ((1ull << u) - 1ull));
-          if (y.L + dep >= raw_lo) extra_mask |= 1u << u;
-        }
-        if ((v4 >> u) & 1ull) extra_mask |= 1u << (kDp + u);
-        if ((v128 >> u) & 1ull) extra_mask |= 1u << (2 * kDp + u);
-      }
-    }
+    bool masks = false;
+    auto load_masks = [&]() {
+      const uint64_t rm = row_masks(p, b, row_ok ? grow : -1, y.L, !waited);
+      waited = true;
+      masks = true;
+      raw_lo = (int)(rm >> 32);
+      extra_mask = (uint32_t)rm;
+    };
+    if (waited) load_masks();
 
     float m_ref = -INFINITY, l_run = 0.f;
     // The two warps of a row (column halves) meet at one named barrier per tile.  A warp whose
@@ -952,6 +1003,7 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
         // visible columns of this thread as a 64-bit mask: a range [lo, hi) of the tile's
         // entries (prefix tiles: all valid entries; raw tiles: positions >= raw_lo), or the
         // extra tile's per-node bits.  One code path for every tile kind.
+        if (kOverlap && x.kind >= kRaw && !masks) load_masks();
         uint64_t vmask;
         if (x.kind == kExtra) {
           vmask = c0 == 0 ? (uint64_t)extra_mask : 0ull;
@@ -1055,6 +1107,7 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
       const int mb = (q - 1) & 1;
       st_async_v2(mapa_cluster(smem_u32(&sm.h.ml[mb][row][0]), partner), __float_as_uint(m_ref),
                   __float_as_uint(l_tot), mapa_cluster(smem_u32(&sm.h.ml_full[mb]), partner));
+      if (kOverlap) pdl_wait_once(waited);   // no write before the kernel depended on completed
       if (row_ok && p.n_chunks == 1)
         p.lse[(int64_t)b * p.DH + grow] =
             l_tot > 0.f ? (m_ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
@@ -1064,6 +1117,7 @@ __device__ void softmax_s(const Params& p, Smem& sm, uint32_t rank) {
 
 // ---- pair O role warps: per-tile rescale, then each item's epilogue ------------------------------
 // Warp w (2..9) serves lane quadrant w % 4 and O columns 256ch .. 256ch+255, ch = (w-2)/4.
+template <bool kOverlap>
 __device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -1074,14 +1128,16 @@ __device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
   const bool arms = row == 0 && ch == 0;   // the thread that arms the receiving barriers
   const int d = 512;
   int g = 0, q = 0;
+  bool waited = !kOverlap;   // (without the overlap the prologue waited)
   Item it;
-  for (int k = 0; item_at(p, k, rank & 1u, it); ++k) {
+  for (int k = 0; item_at(p, sm, k, rank & 1u, it); ++k) {
     const int n = it.te - it.tb;
     const int b = it.b;
     const int grow = 128 * it.rt + row;
     const bool row_ok = grow < p.DH;
     if (n <= 0) {
       if (it.y.T > 0 && p.n_chunks > 1 && row_ok) {   // an empty KV chunk: l = 0
+        if (kOverlap) pdl_wait_once(waited);   // no write before the kernel depended on completed
         float* prow = p.part + part_row(p, b, grow, it.chunk) * (d + 4);
         for (int c = 0; c < 256; c += 4)
           *reinterpret_cast<float4*>(prow + 256 * ch + c) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1136,6 +1192,9 @@ __device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
     }
     ++q;
     tc_fence_after();
+    // no write before the kernel this one depends on has completed (at once here: the item's
+    // extra tile was loaded after that wait)
+    if (kOverlap) pdl_wait_once(waited);
     const float m = sm.h.ml[mb][row][0], l = sm.h.ml[mb][row][1];
     if (p.n_chunks == 1) {
       // O leaves through shared memory and TMA stores: the V ring (idle from o_full until this
@@ -1219,8 +1278,10 @@ __device__ void rescale_epilogue_o(const Params& p, Smem& sm, uint32_t rank) {
 
 // kPaged: the persistent cache is in page pools (C4 tiles through the page table, C128 entries
 // and the raw tail from gathered copies); a separate instantiation keeps the contiguous path's
-// producer free of the page-table work.
-template <bool kPaged>
+// producer free of the page-table work.  kOverlap: the launch chain's overlap with the kernel
+// before this one (the kernel ranks the requests itself and waits late); without it, the
+// instantiation waits in its prologue and keeps the late-wait checks out of its tile loops.
+template <bool kPaged, bool kOverlap>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
@@ -1232,6 +1293,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   }
   pdl_launch_dependents();   // the acceptance walk reads nothing this kernel writes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (kOverlap && warp >= 2) {
+    // the requests' lengths and tile counts for the ranking below, read through L2 (there is no
+    // dependency wait before this read; the kernel before this one does not write L) by the
+    // role warps while warps 0 and 1 set up the barriers and TMEM
+    for (int j = (int)threadIdx.x - 64; j < p.B; j += (int)blockDim.x - 64) {
+      const int L = __ldcg(p.L + j);
+      sm.h.len[j] = L;
+      sm.h.tiles[j] = (uint16_t)min(layout_for(p, L).T, 65535);
+    }
+  }
   // clusters of 4 consecutive CTAs; rank = 2 * (0: pair S, 1: pair O) + (row tile & 1)
   const uint32_t rank = blockIdx.x & 3;
   const bool role_s = rank < 2;
@@ -1277,12 +1348,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   tc_fence_before();
   cluster_sync();   // every CTA's barriers exist before any remote arrive, store or pair MMA
   tc_fence_after();
-  // launched as a programmatic dependent of the scheduling kernel: the set-up above overlaps it;
-  // every read of the round's inputs comes after it has completed
-  pdl_wait();
+  if (kOverlap) {
+    // rank the requests here (longest first, ties by index; the same order as order_kernel);
+    // the cluster barrier above made every thread's tile counts visible
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+      const int tb = sm.h.tiles[b];
+      int r = 0;
+      for (int j = 0; j < p.B; ++j) {
+        const int tj = sm.h.tiles[j];
+        r += (tj > tb || (tj == tb && j < b)) ? 1 : 0;
+      }
+      sm.h.order[r] = (uint16_t)b;
+    }
+    __syncthreads();
+  } else {
+    // a programmatic dependent of the ranking kernel: the set-up above overlaps it; every read
+    // of the round's inputs comes after it has completed
+    pdl_wait();
+  }
 
   if (warp == 0) {
-    producer<kPaged>(p, sm, role_s, sub);
+    producer<kPaged, kOverlap>(p, sm, role_s, sub);
   } else if (warp == 1) {
     if (lane == 0 && sub == 0) {
       if (role_s)
@@ -1300,11 +1386,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
     __syncwarp();
   } else if (role_s) {
-    softmax_s(p, sm, rank);
+    softmax_s<kOverlap>(p, sm, rank);
   } else {
-    rescale_epilogue_o(p, sm, rank);
+    rescale_epilogue_o<kOverlap>(p, sm, rank);
   }
 
+  if (kOverlap) pdl_wait();   // this kernel completes only after the one it depends on
   tc_fence_before();
   cluster_sync();   // the leaders' MMAs are drained; every awaited remote store has landed
   // after that barrier all four CTAs see the same abort flag (fail() sets the others' flags
@@ -1372,10 +1459,12 @@ int cluster_slots() {
   if (slots[dev] == 0) {
     using namespace tv::tc;
     const int smem = (int)sizeof(Smem);
-    if (cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(attn_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_kernel<false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_kernel<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
@@ -1391,7 +1480,8 @@ int cluster_slots() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<false>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<false, false>, &cfg) != cudaSuccess ||
+        n <= 0) {
       cudaGetLastError();
       int sms = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -1587,7 +1677,9 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   p.O = a.O;
   p.lse = a.lse;
   int32_t* order = reinterpret_cast<int32_t*>(workspace);
-  p.order = order;
+  // null: ranked in the kernel's prologue, which then overlaps the kernel before it (the
+  // contiguous dense path; a gather of selected or paged rows comes first otherwise)
+  p.order = (s->B <= kRankMax && !gathered && !paged) ? nullptr : order;
   p.part = reinterpret_cast<float*>(ws + pre_partial_bytes(s));
   p.status = a.status;
   p.timeout_ns = (uint64_t)g_timeout_ns.load();
@@ -1612,11 +1704,13 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
         reinterpret_cast<uint4*>(graw + paged_raw_bytes(s)), a.status);
     if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 paged gather)")) return rc;
   }
-  // one CTA ranks all requests (B <= 12288 fits its default shared memory)
-  if (tv::launch_pdl(order_kernel, dim3(1), dim3(1024), (size_t)s->B * sizeof(int), stream, p,
-                 order) != cudaSuccess)
-    return tv_check_launch("tv_tree_verify_attn (tcgen05 schedule launch)");
-  if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;
+  // larger batches: one CTA ranks all requests (B <= 12288 fits its default shared memory)
+  if (p.order != nullptr) {
+    if (tv::launch_pdl(order_kernel, dim3(1), dim3(1024), (size_t)s->B * sizeof(int), stream, p,
+                       order) != cudaSuccess)
+      return tv_check_launch("tv_tree_verify_attn (tcgen05 schedule launch)");
+    if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05 schedule)")) return rc;
+  }
   if (cluster_slots() <= 0)
     return tv_check_launch("tv_tree_verify_attn (tcgen05 kernel attributes)");
   const size_t smem = sizeof(Smem);
@@ -1634,12 +1728,13 @@ int tv_launch_attn_tc(const tv_shape* s, const tv::AttnParams<__nv_bfloat16>& a,
   attr[0].val.clusterDim.x = kClusterCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // after the schedule
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see the launch chain
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t le = paged ? cudaLaunchKernelEx(&cfg, attn_kernel<true>, p)
-                               : cudaLaunchKernelEx(&cfg, attn_kernel<false>, p);
+  const cudaError_t le = paged                ? cudaLaunchKernelEx(&cfg, attn_kernel<true, false>, p)
+                         : p.order == nullptr ? cudaLaunchKernelEx(&cfg, attn_kernel<false, true>, p)
+                                              : cudaLaunchKernelEx(&cfg, attn_kernel<false, false>, p);
   if (le != cudaSuccess)
     return tv_check_launch("tv_tree_verify_attn (tcgen05 cluster launch)");
   if (int rc = tv_check_launch("tv_tree_verify_attn (tcgen05)")) return rc;
