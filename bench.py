@@ -795,17 +795,18 @@ def run_draft(args):
 
 def launches_per_step(shape, kernel):
     # plan, branch compress, accept, refresh + attention: SIMT (partials, merge; + the indexer's
-    # score and select kernels on the sparse path) or tensor cores
-    # (selection gather when a C4 selection list is given, request ranking, pair kernel, merge
-    # when the KV is split)
+    # score and select kernels on the sparse path) or tensor cores (selection gather when a C4
+    # selection list is given, request ranking, pair kernel, merge when the KV is split)
     from tree_speculative_verify_gb300 import _lib
     if kernel == "simt":
         return 6 + (2 if shape.n_sel > 0 else 0)
     gather = shape.B * shape.n_sel * 512 * 2 * 2
     split = _lib.tv_workspace_size(shape) > ((shape.B * 4 + 255) // 256) * 256 + gather
-    # + the indexer's score and select kernels and the selection gather on the sparse path, and
-    # the gather of the C128 entries and raw tails from page pools
-    return (4 + 2 + (1 if split else 0) + (3 if shape.n_sel > 0 else 0)
+    # the ranking kernel runs unless the attention ranks the requests itself (contiguous dense
+    # path, B <= 2048); + the indexer's score and select kernels and the selection gather on the
+    # sparse path, and the gather of the C128 entries and raw tails from page pools
+    ranking = shape.n_sel > 0 or shape.page_tokens > 0 or shape.B > 2048
+    return (4 + 1 + (1 if ranking else 0) + (1 if split else 0) + (3 if shape.n_sel > 0 else 0)
             + (1 if shape.page_tokens > 0 else 0))
 
 
