@@ -20,6 +20,12 @@
  *   returns TV_OK once its kernels are enqueued, or a negative TV_ERR_* code, without launching
  *   anything, when the host-side arguments are invalid (null pointer, bad shape).  The reason of
  *   the last host-side error of the calling thread is available from tv_last_error_string().
+ * - Stream order holds as for ordinary launches.  Inside the library, kernels are launched as
+ *   programmatic dependents of the kernel before them and start early only after one of this
+ *   library's own kernels that allows it; each waits before it reads that kernel's results or
+ *   writes anything, and before it completes.  A caller's kernel placed just before a call and
+ *   itself allowing early starts (griddepcontrol.launch_dependents) must not write the call's
+ *   inputs after that point.
  * - Errors found on the device (a malformed tree, a capacity overflow, a bad selection index,
  *   a wait that ran out) are written to the caller's int32 *status word with first-error-wins
  *   semantics (the word is only ever changed from 0 to a negative code); read it after the
