@@ -34,9 +34,10 @@ __global__ void accept_kernel(int B, int D, const int32_t* __restrict__ parents,
   if (v0 < D) ok &= (v0 == 0) ? (p0 == -1) : (p0 >= 0 && p0 < v0);
   if (v1 < D) ok &= (p1 >= 0 && p1 < v1);
   // launched as a programmatic dependent of the attention: the inputs above are not written by
-  // it; the outputs below wait for the kernel before this one to complete
-  pdl_wait();
+  // it, and the walk runs in registers; the stores below wait for the kernel before this one to
+  // complete
   if (!__all_sync(0xffffffffu, ok)) {
+    pdl_wait();
     if (lane == 0) {
       record_error(status, TV_ERR_BAD_TREE);
       accept_len[b] = 1;
@@ -60,9 +61,10 @@ __global__ void accept_kernel(int B, int D, const int32_t* __restrict__ parents,
     ++n;
     cur = nxt;
   }
+  const int bonus_tok = __shfl_sync(0xffffffffu, cur < 32 ? t0 : t1, cur & 31);
+  pdl_wait();
   if (v0 < D) path[base + v0] = my0;
   if (v1 < D) path[base + v1] = my1;
-  const int bonus_tok = __shfl_sync(0xffffffffu, cur < 32 ? t0 : t1, cur & 31);
   if (lane == 0) {
     accept_len[b] = n;
     bonus[b] = bonus_tok;
