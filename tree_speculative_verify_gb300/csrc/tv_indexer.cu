@@ -18,11 +18,13 @@
 //   select_kernel, a cluster of eight CTAs per request, CTA r owning the request's r-th contiguous
 //   eighth of the entries (their order-preserving keys staged in shared memory):
 //   2. an 8-bit-digit radix select of the n_sel-th largest key over the whole request: per pass
-//      every CTA counts its keys into a shared-memory histogram, and after one cluster barrier each
-//      CTA sums the eight histograms through distributed shared memory and picks the same digit;
+//      every CTA counts its keys into a shared-memory histogram and stores it into every rank's
+//      shared memory (distributed shared memory), and after one cluster barrier each CTA adds the
+//      eight histograms up locally and picks the same digit;
 //   3. the kept entries in ascending order: every warp counts the entries above the threshold and
-//      the ties in its contiguous index range, CTAs in rank order and warps in index order place
-//      them (ties: the lowest indices), and each warp writes its own.
+//      the ties in its contiguous index range, CTAs in rank order (each pushes its counts to the
+//      higher ranks before one last cluster barrier) and warps in index order place them (ties:
+//      the lowest indices), and each warp writes its own.
 //   The select kernel is a programmatic dependent of the score kernel: its launch overlaps the
 //   scoring, and it waits for the scores before it reads them.
 #include <cooperative_groups.h>
@@ -134,11 +136,13 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) uint32_t keys[];   // this CTA's keys (when staged)
-  __shared__ unsigned hist[2][256];   // by pass parity (a rank that runs ahead never clears a
-                                      // histogram a slower rank still reads)
+  __shared__ unsigned hist[256];      // this CTA's histogram of the pass
+  // every rank's histogram of the pass, pushed here by that rank; by pass parity, so that a rank
+  // that runs ahead never overwrites a histogram this CTA still adds up
+  __shared__ unsigned hall[2][kTopkRanks][256];
   __shared__ unsigned ghist[256];     // the pass's histogram of the whole request
   __shared__ int warp_gt[kTopkWarps], warp_eq[kTopkWarps];
-  __shared__ int cta_gt, cta_eq;
+  __shared__ int2 before[kTopkRanks];  // (above, equal) counts of the lower ranks, pushed by them
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_krem;
   pdl_wait();   // the scores are complete and visible
@@ -166,6 +170,7 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
     s_mask = 0u;
     s_krem = n_sel;
   }
+  if (tid < 256) hist[tid] = 0u;
   // 1. this CTA's keys (the padding up to whole 16-byte vectors: key 0, never counted)
   if (staged) {   // all of a thread's loads in flight at once
     constexpr int kPerThread = (kStageKeys + kTopkThreads - 1) / kTopkThreads;
@@ -187,11 +192,9 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
   // 2. radix select of the n_sel-th largest key of the request, most significant digit first
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass, par = pass & 1;
-    for (int i = tid; i < 256; i += blockDim.x) hist[par][i] = 0u;
-    __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
     auto count = [&](uint32_t key) {
-      if ((key & mask) == prefix) atomicAdd(&hist[par][(key >> shift) & 255u], 1u);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
     };
     if (staged) {
       const uint4* k4 = reinterpret_cast<const uint4*>(keys);
@@ -207,14 +210,17 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
       for (int j = lo + tid; j < hi; j += blockDim.x) count(score_key(sc[j]));
     }
     __syncthreads();
-    cl.sync();   // every rank's histogram of this pass is complete
-    if (tid < 256) {   // bin tid summed over the ranks (their loads in flight together)
-      unsigned v[kTopkRanks];
+    if (tid < 256) {   // bin tid to every rank (stores, none awaited), then cleared for the next pass
+      const unsigned h = hist[tid];
 #pragma unroll
-      for (int r = 0; r < kTopkRanks; ++r) v[r] = *cl.map_shared_rank(&hist[par][tid], r);
+      for (int r = 0; r < kTopkRanks; ++r) *cl.map_shared_rank(&hall[par][rank][tid], r) = h;
+      hist[tid] = 0u;
+    }
+    cl.sync();   // every rank's histogram of this pass has arrived
+    if (tid < 256) {   // bin tid summed over the ranks, in rank order
       unsigned t = 0u;
 #pragma unroll
-      for (int r = 0; r < kTopkRanks; ++r) t += v[r];
+      for (int r = 0; r < kTopkRanks; ++r) t += hall[par][r][tid];
       ghist[tid] = t;
     }
     __syncthreads();
@@ -270,29 +276,20 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
     warp_eq[warp] = eq;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0) {   // this CTA's counts to every higher rank
     int a = 0, e = 0;
     for (int w = 0; w < kTopkWarps; ++w) {
       a += warp_gt[w];
       e += warp_eq[w];
     }
-    cta_gt = a;
-    cta_eq = e;
+    for (int r = rank + 1; r < kTopkRanks; ++r)
+      *cl.map_shared_rank(&before[rank], r) = make_int2(a, e);
   }
-  cl.sync();   // every rank's counts are visible
+  cl.sync();   // every lower rank's counts have arrived (the last access to a peer's memory)
   int gt_before = 0, eq_before = 0;
-  {
-    int g[kTopkRanks], e[kTopkRanks];
-#pragma unroll
-    for (int r = 0; r < kTopkRanks; ++r) {
-      g[r] = r < rank ? *cl.map_shared_rank(&cta_gt, r) : 0;
-      e[r] = r < rank ? *cl.map_shared_rank(&cta_eq, r) : 0;
-    }
-#pragma unroll
-    for (int r = 0; r < kTopkRanks; ++r) {
-      gt_before += g[r];
-      eq_before += e[r];
-    }
+  for (int r = 0; r < rank; ++r) {
+    gt_before += before[r].x;
+    eq_before += before[r].y;
   }
   for (int w = 0; w < warp; ++w) {
     gt_before += warp_gt[w];
@@ -311,7 +308,6 @@ __global__ void __cluster_dims__(kTopkRanks, 1, 1) __launch_bounds__(kTopkThread
     pos += __popc(tm);
     eq_seen += __popc(eqm);
   }
-  cl.sync();   // no CTA leaves while a peer may still read its counts
 }
 
 }  // namespace
